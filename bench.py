@@ -1,0 +1,359 @@
+"""Benchmark of the absorbed-MLA decode step on GB300.
+
+One step = the whole hot path on one synthetic decode batch:
+  mla_cache_write of the step's new latent rows (one per query token), then
+  mla_decode (split-KV plan, tcgen05 decode, LSE combine).
+Default workload: DeepSeek-V3-shaped decode, N=128 heads, batch 64, contexts
+uniform in [1024, 8192], page 64, bf16 cache in a 40k-page pool.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                       [--workload NAME]
+Prints one JSON line.  With --gpus N > 1 (under torchrun) every rank runs an
+independent replica (the decode of one batch does not shard), value = tokens of
+all ranks / max time over ranks.  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MLA decode tokens/s + HBM GB/s & % roofline (N=128,B=64,ctx 4k,bf16)"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic(case):
+    """Bytes and FLOPs the decode must move / do at minimum: every visible
+    latent row read once per request, queries read, outputs and LSE written;
+    2*(576+512) FLOP per (visible key, query row)."""
+    N = case.num_heads
+    row_bytes = synth.DQK * (2 if case.cache_dtype == "bf16" else 1)
+    kv = int(case.seq_lens.clip(min=0).sum()) * row_bytes
+    T = case.total_q
+    q = T * N * synth.DQK * 2
+    out = T * N * synth.LKV * 2 + T * N * 4
+    qsl = case.query_start_loc
+    vis = 0
+    for b in range(case.batch):
+        sq = int(qsl[b + 1] - qsl[b])
+        for t in range(sq):
+            vis += max(int(case.seq_lens[b]) - sq + 1 + t, 0)
+    flops = 2 * (synth.DQK + synth.LKV) * N * vis
+    write = T * (synth.DQK * 2 + row_bytes)           # new rows read + cache rows written
+    return dict(kv=kv, q=q, out=out, decode_bytes=kv + q + out, write_bytes=write, flops=flops)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.dev), "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gpu(args):
+    import torch
+    import mla_latent_kv_15_gb300 as mla
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    mla.load()
+
+    case = synth.workload(args.workload, poison=False)
+    N, T, B = case.num_heads, case.total_q, case.batch
+    dev = "cuda"
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # resident state: the paged cache
+    if case.cache_dtype == "bf16":
+        cache = bf16(case.pool)
+    else:
+        cache = torch.zeros(case.pool.shape, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+        flat = case.pool.reshape(-1, synth.DQK)[case.referenced_slots]
+        mla.cache_write(bf16(flat[:, :synth.LKV]), bf16(flat[:, synth.LKV:]),
+                        torch.from_numpy(case.referenced_slots).to(dev), cache, case.kv_scale)
+    # per-step inputs (device copies) and their pinned host twins for the e2e leg
+    host = {
+        "q_abs": torch.from_numpy(case.q_abs.view(np.int16)).view(torch.bfloat16),
+        "q_pe": torch.from_numpy(case.q_pe.view(np.int16)).view(torch.bfloat16),
+        "kv_c": torch.from_numpy(case.new_kv_c.view(np.int16)).view(torch.bfloat16),
+        "k_pe": torch.from_numpy(case.new_k_pe.view(np.int16)).view(torch.bfloat16),
+        "slots": torch.from_numpy(case.slot_mapping),
+        "block_table": torch.from_numpy(case.block_table),
+        "seq_lens": torch.from_numpy(case.seq_lens),
+        "qsl": torch.from_numpy(case.query_start_loc),
+    }
+    host = {k: v.pin_memory() for k, v in host.items()}
+    d = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty((T, N, synth.LKV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(mla.decode_workspace_size(B, T, N, args.num_splits), dtype=torch.uint8, device=dev)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(inp):
+        mla.cache_write(inp["kv_c"], inp["k_pe"], inp["slots"], cache, case.kv_scale)
+        mla.decode(inp["q_abs"], inp["q_pe"], cache, inp["block_table"], inp["seq_lens"], out, ws,
+                   scale=case.scale, query_start_loc=inp["qsl"], lse=lse, num_splits=args.num_splits,
+                   kv_scale=case.kv_scale)
+
+    for _ in range(args.warmup):
+        step(d)
+    torch.cuda.synchronize()
+    status = mla.decode_status(ws)
+    if status != 0:
+        raise RuntimeError(f"decode reported device error word {status}")
+
+    # ---- timed region: device-resident inputs, L2 flushed before every step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in kev:          # torch creates its events lazily: record once so the handles exist
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            mla.set_decode_timing_events(*kev[i])
+            ev[i][0].record(stream)
+            step(d)
+            ev[i][1].record(stream)
+        mla.set_decode_timing_events(None, None)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    ms = sum(step_ms) / len(step_ms)
+    kms = sum(kern_ms) / len(kern_ms)
+
+    # ---- e2e: host (pinned) inputs copied in and outputs copied out every step
+    inp_bytes = sum(v.numel() * v.element_size() for v in host.values())
+    out_bytes = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        for k in d:
+            d[k].copy_(host[k], non_blocking=True)
+        step(d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+
+    if dist:
+        t = torch.tensor([ms, kms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kms, e2e_ms = t.tolist()
+    if rank != 0:
+        return None
+
+    alg = algorithmic(case)
+    hbm, tflops, src = peaks()
+    achieved = alg["decode_bytes"] / (kms * 1e-3) / 1e9
+    tok_s = world * T / (ms * 1e-3)
+    clocks = sampler.summary()
+    res = {
+        "metric": METRIC,
+        "value": round(tok_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.cache_dtype == "bf16" else "e4m3-cache/bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload, "num_heads": N, "batch": B, "total_q": T,
+            "ctx_sum": int(case.seq_lens.sum()), "page_size": case.page_size, "num_blocks": case.num_blocks,
+            "cache_dtype": case.cache_dtype, "num_splits": args.num_splits, "parallelism": f"replicas{world}",
+            "l2": "flushed (256 MiB write) before every timed step",
+        },
+        "hbm_gbs": round(achieved, 1),
+        "tflops": round(alg["flops"] / (kms * 1e-3) / 1e12, 1),
+        "decode_kernel_ms": round(kms, 5),
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": None,
+            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
+            "algorithmic_bytes_per_launch": alg["decode_bytes"],
+        },
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": inp_bytes, "d2h_bytes_per_step": out_bytes},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    return res
+
+
+def cpu_baseline(case, seconds: float):
+    """The fp64 oracle on the host cores over a bounded sample of the workload:
+    whole requests (all heads, full contexts) until ~`seconds` of work."""
+    import oracle
+    cache = oracle.prepare_cache(case)
+    N = case.num_heads
+    qsl = case.query_start_loc
+    done_tokens = 0
+    t0 = time.perf_counter()
+    cores = 0
+    b = 0
+    while b < case.batch and (time.perf_counter() - t0) < seconds:
+        rows = np.arange(qsl[b] * N, qsl[b + 1] * N, dtype=np.int64)
+        _, _, cores = oracle.decode_case(case, cache, rows=rows)
+        done_tokens += int(qsl[b + 1] - qsl[b])
+        b += 1
+    el = time.perf_counter() - t0
+    return {"value": round(done_tokens / el, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{b} of {case.batch} requests (all {N} heads, full contexts), {el:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle as it stands on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    case = synth.workload(args.workload, poison=False)
+    cache = oracle.prepare_cache(case)
+    N = case.num_heads
+    qsl = case.query_start_loc
+    per_step = max(1, args.ref_requests)
+    times, cores = [], 0
+    b = 0
+    for i in range(args.warmup + args.steps):
+        reqs = [(b + k) % case.batch for k in range(per_step)]
+        b += per_step
+        rows = np.concatenate([np.arange(qsl[r] * N, qsl[r + 1] * N, dtype=np.int64) for r in reqs])
+        t0 = time.perf_counter()
+        _, _, cores = oracle.decode_case(case, cache, rows=rows)
+        el = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append((el, sum(int(qsl[r + 1] - qsl[r]) for r in reqs)))
+    tot = sum(t for t, _ in times)
+    toks = sum(n for _, n in times)
+    v = toks / tot
+    return {
+        "metric": METRIC, "impl": "reference", "value": round(v, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * tot / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "num_heads": N, "batch": case.batch,
+                   "sample_per_step": f"{per_step} request(s), all heads, full contexts"},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} request(s) per step x {args.steps} steps"},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="dsv3_n128_b64_ctx1k-8k", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-requests", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

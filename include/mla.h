@@ -1,0 +1,200 @@
+/*
+ * mla.h -- C ABI of libmla.so: absorbed ("data-movement friendly") Multi-head
+ * Latent Attention decode over a paged latent KV cache, for NVIDIA GB300
+ * (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers to dense, row-major tensors
+ *    (no strides) that the caller allocates and owns.  The library keeps no
+ *    pointer after a call returns and allocates no memory: scratch memory
+ *    comes from the caller (`workspace`).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Every call is asynchronous with respect to the host: it only
+ *    enqueues kernels on `stream`.
+ *  - Return value: MLA_OK (0) or a negative mla_status.  Arguments are
+ *    validated on the host BEFORE anything is enqueued; on an error nothing
+ *    is launched and mla_last_error() describes the problem.  Device-side
+ *    data (slot ids, block-table entries, sequence lengths) cannot be checked
+ *    on the host; how each call treats bad values is stated below.
+ *  - Latent widths are fixed by the model family: Lkv = 512 (kv_c / q_abs /
+ *    output), R = 64 (k_pe / q_pe), cache row = Lkv + R = 576 elements
+ *    (vllm/v1/attention/backends/mla/common.py, module docstring, "More
+ *    Extent Definitions", DeepSeek-V3 values).
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size or enum    */
+  MLA_ERR_UNSUPPORTED = -2, /* valid request outside what the kernels cover  */
+  MLA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed             */
+  MLA_ERR_WORKSPACE = -4    /* workspace missing or smaller than required   */
+};
+
+enum mla_dtype {
+  MLA_BF16 = 0,     /* bfloat16                                        */
+  MLA_FP8_E4M3 = 1, /* OCP FP8 E4M3 ("fn": no inf, max 448)            */
+  MLA_FP32 = 2      /* float32 (merge inputs/outputs only)              */
+};
+
+/* Device error word bits written by mla_decode (see mla_decode_status). */
+enum mla_device_error {
+  MLA_DEVERR_TIMEOUT = 1,       /* a bounded on-chip wait gave up          */
+  MLA_DEVERR_BAD_SEQ_LEN = 2,   /* seq_len > max_pages_per_seq*page_size   */
+  MLA_DEVERR_BAD_BLOCK = 4,     /* block-table entry outside [0,num_blocks) */
+  MLA_DEVERR_BAD_QSL = 8        /* query_start_loc inconsistent with total_q */
+};
+
+/*
+ * mla_cache_write -- concat_and_cache_mla: store the latent rows of new tokens
+ * in the paged cache (common.py, MLACommonImpl.forward, "write the latent and
+ * rope to kv cache"; mla_attention.py, MLAAttention.forward ->
+ * do_kv_cache_update).
+ *
+ *   kv_c          [num_tokens, 512] bf16, 16-byte aligned
+ *   k_pe          [num_tokens, 64]  bf16, 16-byte aligned
+ *   slot_mapping  [num_tokens] int64: flattened cache row of each token,
+ *                 slot = block * page_size + offset_in_block; a negative slot
+ *                 marks a padding token and is skipped.  Slots >= num_blocks *
+ *                 page_size are skipped as well (device data is not checked
+ *                 on the host).
+ *   cache         [num_blocks, page_size, 576] of cache_dtype, 16-byte aligned;
+ *                 row `slot` receives [kv_c | k_pe].
+ *   cache_dtype   MLA_BF16: the bf16 bits are copied unchanged.
+ *                 MLA_FP8_E4M3: each value x is stored as e4m3(x / kv_scale),
+ *                 float32 divide, round to nearest even, finite overflow
+ *                 saturated to +-448 (kv_scale = abs-max / 448 as in
+ *                 calc_kv_scales; dequantisation multiplies by kv_scale).
+ *   kv_scale      > 0 and finite for fp8; ignored for bf16.
+ * num_tokens == 0 is a no-op.  One launch.
+ */
+MLA_API int mla_cache_write(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_tokens,
+                    void* cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
+                    void* stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of device workspace mla_decode needs for
+ * a batch of `batch` requests, `total_q` query tokens in all, `num_heads`
+ * heads, and a split count num_splits <= max_splits (pass 0 when only the
+ * automatic split is used).  Depends on sizes only, never on device data, so
+ * a buffer sized once serves every later step of the same shape (and every
+ * CUDA-graph replay).
+ */
+MLA_API size_t mla_decode_workspace_size(int batch, int total_q, int num_heads, int max_splits);
+
+/*
+ * mla_decode -- absorbed MLA decode (forward_mqa): for every query row
+ * (token t, head h) attend, as MQA, over the request's latent rows
+ * [kv_c | k_pe] reached through its block table, and return the 512-wide
+ * latent output and the natural-log LSE (common.py docstring,
+ * "Data-Movement Friendly Approach"; mla_attention.py MLACommonImpl.forward_mqa
+ * returns (o, lse)):
+ *
+ *   s_j   = scale * (q_abs[t,h] . kv_c_j + q_pe[t,h] . k_pe_j)
+ *   out   = sum_j softmax(s)_j * kv_c_j          lse = ln sum_j exp(s_j)
+ *
+ * over keys j < L(t) = seq_len[b] - Sq_b + 1 + t_local: with Sq_b query tokens
+ * a request's t-th verify token sees its context plus the new tokens up to
+ * itself (rocm_aiter_mla.py, AiterMLAImpl.forward_mqa, multi-token verify).
+ * Long contexts are split across CTAs and recombined with the LSE merge
+ * (merge_attn_states).  Rows with L(t) <= 0 (e.g. seq_len 0 padding requests)
+ * get out = 0 and lse = -inf.
+ *
+ *   q_abs            [total_q, num_heads, 512] bf16 (ql_nope = q_nope . W_UK)
+ *   q_pe             [total_q, num_heads, 64]  bf16
+ *   cache            [num_blocks, page_size, 576] of cache_dtype (bf16 or e4m3)
+ *   kv_scale         fp8 dequantisation scale (row value = code * kv_scale);
+ *                    ignored for bf16
+ *   block_table      [batch, max_pages_per_seq] int32: physical block of each
+ *                    logical page; token j of request b is row
+ *                    block_table[b, j / page_size] * page_size + j % page_size
+ *   seq_lens         [batch] int32: tokens of each request INCLUDING its query
+ *                    tokens of this step
+ *   query_start_loc  [batch + 1] int32 prefix sums of per-request query counts
+ *                    (query_start_loc[0] = 0, [batch] = total_q), or NULL for
+ *                    one query token per request (then total_q == batch)
+ *   num_heads        1..1024
+ *   scale            softmax scale, passed explicitly (1/sqrt(P+R) for MLA)
+ *   num_splits       0: split long contexts automatically to balance all SMs;
+ *                    k > 0: cut every (request, 128-row group) into
+ *                    min(k, tiles) contiguous pieces of near-equal length
+ *   out              [total_q, num_heads, 512] bf16
+ *   lse              [total_q, num_heads] float32, or NULL
+ *   workspace        >= mla_decode_workspace_size(batch, total_q, num_heads,
+ *                    num_splits) bytes, 256-byte aligned; scratch only
+ *   page_size        16, 32, 64, 128 or 256
+ * All device pointers 16-byte aligned.  Launches: a scheduler kernel, the
+ * decode kernel and a combine kernel.  Device data errors (seq_len beyond
+ * the block table, block ids outside the cache) do not fault: the affected
+ * rows read zeros and a bit of mla_device_error is set in the workspace's
+ * status word (mla_decode_status).
+ */
+MLA_API int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks, int page_size,
+               int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+               const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q,
+               int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/*
+ * mla_decode_status -- copy the device error word of the last mla_decode that
+ * used `workspace` (OR of mla_device_error bits; 0 = clean) to *status.
+ * Synchronises `stream`.  The word is cleared by every mla_decode.
+ */
+MLA_API int mla_decode_status(const void* workspace, int* status, void* stream);
+
+/*
+ * mla_merge_states -- merge_attn_states: combine two partial attention
+ * results over disjoint key sets (common.py docstring, "Chunked Prefill";
+ * MLACommonImpl._compute_prefill_context):
+ *
+ *   lse = ln(exp(lse_a) + exp(lse_b))
+ *   out = exp(lse_a - lse) * o_a + exp(lse_b - lse) * o_b
+ *
+ * A side with lse = -inf (no keys) gets weight 0; both -inf gives out = 0,
+ * lse = -inf.
+ *   o_a, o_b, out   [rows, dim] of o_dtype (MLA_BF16 or MLA_FP32)
+ *   lse_a, lse_b    [rows] float32 natural-log LSE
+ *   lse_out         [rows] float32, or NULL; must not alias lse_a or lse_b
+ *   dim             multiple of 8, <= 4096
+ * rows == 0 is a no-op.  out may alias o_a or o_b.  One launch.
+ */
+MLA_API int mla_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, int64_t rows,
+                     int dim, int o_dtype, void* out, float* lse_out, void* stream);
+
+/*
+ * mla_set_decode_timing_events -- profiling aid.  While both events are
+ * non-NULL, every later mla_decode call of the calling thread records `start`
+ * immediately before and `stop` immediately after its decode kernel, on the
+ * call's stream, so the kernel can be timed alone with cudaEventElapsedTime.
+ * The events (cudaEvent_t passed as void*) belong to the caller.  Passing NULL
+ * for either turns the recording off.  Always returns MLA_OK.
+ */
+MLA_API int mla_set_decode_timing_events(void* start, void* stop);
+
+/* Human-readable description of the calling thread's last error ("" if none). */
+MLA_API const char* mla_last_error(void);
+
+/* Streaming multiprocessors of the current device (the decode grid is sized
+ * from it), or a negative mla_status. */
+MLA_API int mla_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

@@ -1,0 +1,147 @@
+"""Python binding of libmla.so: absorbed MLA decode over a paged latent KV cache
+on GB300 (sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels,
+reached through its C ABI (``include/mla.h``) with ctypes.  PyTorch provides
+device memory and streams.  There is no fallback: if ``libmla.so`` is missing
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmla.so")
+
+MLA_OK = 0
+MLA_BF16 = 0
+MLA_FP8_E4M3 = 1
+MLA_FP32 = 2
+DEVERR_TIMEOUT = 1
+DEVERR_BAD_SEQ_LEN = 2
+DEVERR_BAD_BLOCK = 4
+DEVERR_BAD_QSL = 8
+LKV = 512
+ROPE = 64
+DQK = 576
+
+C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
+                 "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events")
+
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmla.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.mla_cache_write.restype = i32
+    lib.mla_cache_write.argtypes = [P, P, P, i64, P, i64, i32, i32, f32, P]
+    lib.mla_decode_workspace_size.restype = sz
+    lib.mla_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.mla_decode.restype = i32
+    lib.mla_decode.argtypes = [P, P, P, i64, i32, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P, sz, P]
+    lib.mla_decode_status.restype = i32
+    lib.mla_decode_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
+    lib.mla_merge_states.restype = i32
+    lib.mla_merge_states.argtypes = [P, P, P, P, i64, i32, i32, P, P, P]
+    lib.mla_last_error.restype = ctypes.c_char_p
+    lib.mla_last_error.argtypes = []
+    lib.mla_device_sm_count.restype = i32
+    lib.mla_device_sm_count.argtypes = []
+    lib.mla_set_decode_timing_events.restype = i32
+    lib.mla_set_decode_timing_events.argtypes = [P, P]
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != MLA_OK:
+        raise MLAError(rc, load().mla_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(cache):
+    import torch
+    if cache.dtype == torch.bfloat16:
+        return MLA_BF16
+    if cache.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return MLA_FP8_E4M3
+    raise TypeError(f"cache dtype {cache.dtype} is neither bf16 nor float8_e4m3fn")
+
+
+def cache_write(kv_c, k_pe, slot_mapping, cache, kv_scale: float = 1.0, stream=None) -> None:
+    """concat_and_cache_mla: cache[num_blocks, page, 576] (bf16 or float8_e4m3fn)."""
+    nb, ps, w = cache.shape
+    assert w == DQK
+    _check(load().mla_cache_write(_ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), slot_mapping.numel(), _ptr(cache),
+                                  nb, ps, _dtype_code(cache), float(kv_scale), _stream(stream)))
+
+
+def decode_workspace_size(batch: int, total_q: int, num_heads: int, max_splits: int = 0) -> int:
+    return int(load().mla_decode_workspace_size(batch, total_q, num_heads, max_splits))
+
+
+def decode(q_abs, q_pe, cache, block_table, seq_lens, out, workspace, *, scale: float,
+           query_start_loc=None, lse=None, num_splits: int = 0, kv_scale: float = 1.0, stream=None) -> None:
+    """Absorbed MLA decode (forward_mqa) into ``out`` [T, N, 512] bf16 and ``lse`` [T, N] fp32."""
+    T, N, _ = q_abs.shape
+    nb, ps, _ = cache.shape
+    B = seq_lens.numel()
+    _check(load().mla_decode(_ptr(q_abs), _ptr(q_pe), _ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale),
+                             _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
+                             T, N, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_status(workspace, stream=None) -> int:
+    st = ctypes.c_int(0)
+    _check(load().mla_decode_status(_ptr(workspace), ctypes.byref(st), _stream(stream)))
+    return st.value
+
+
+def merge_states(o_a, lse_a, o_b, lse_b, out, lse_out=None, stream=None) -> None:
+    """merge_attn_states of two partials (rows x dim, bf16 or fp32)."""
+    import torch
+    rows = lse_a.numel()
+    dim = o_a.numel() // max(rows, 1)
+    code = MLA_BF16 if o_a.dtype == torch.bfloat16 else MLA_FP32
+    _check(load().mla_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, dim, code, _ptr(out),
+                                   _ptr(lse_out), _stream(stream)))
+
+
+def set_decode_timing_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event ``start``/``stop`` around the decode kernel of
+    every later decode() call of this thread (None turns it off)."""
+    sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
+    ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
+    _check(load().mla_set_decode_timing_events(sp, ep))
+
+
+def device_sm_count() -> int:
+    n = load().mla_device_sm_count()
+    if n < 0:
+        _check(n)
+    return n

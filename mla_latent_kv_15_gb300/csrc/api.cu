@@ -1,0 +1,204 @@
+// C-ABI entry points of libmla.so (declared in include/mla.h): host-side
+// argument validation, TMA descriptor encoding and kernel launches.  Nothing
+// here allocates device memory; every buffer belongs to the caller.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/mla.h"
+#include "common.cuh"
+#include "tmap.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+thread_local cudaEvent_t g_timing_start = nullptr, g_timing_stop = nullptr;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return MLA_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  return n;
+}
+
+bool valid_page_size(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 128 || ps == 256; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+int mla_set_decode_timing_events(void* start, void* stop) {
+  g_timing_start = start && stop ? static_cast<cudaEvent_t>(start) : nullptr;
+  g_timing_stop = start && stop ? static_cast<cudaEvent_t>(stop) : nullptr;
+  return ok();
+}
+
+int mla_device_sm_count(void) {
+  int n = sm_count();
+  if (n <= 0) return fail(MLA_ERR_CUDA, "cannot query the current device");
+  return n;
+}
+
+int mla_cache_write(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_tokens,
+                    void* cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
+                    void* stream) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)num_tokens);
+  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
+  if (page_size <= 0 || num_blocks <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "page_size and num_blocks must be positive");
+  if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
+  if (num_tokens == 0) return ok();
+  if (!kv_c || !k_pe || !slot_mapping || !cache) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
+    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe and cache must be 16-byte aligned, slot_mapping 8-byte aligned");
+  cudaError_t e = mla::launch_cache_write(kv_c, k_pe, slot_mapping, num_tokens, cache, num_blocks * page_size,
+                                          cache_dtype == MLA_FP8_E4M3, kv_scale, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
+  return ok();
+}
+
+size_t mla_decode_workspace_size(int batch, int total_q, int num_heads, int max_splits) {
+  if (batch <= 0 || total_q <= 0 || num_heads <= 0 || max_splits < 0) return 0;
+  return mla::workspace_layout(batch, total_q, num_heads, max_splits).total;
+}
+
+int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks, int page_size,
+               int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+               const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q, int num_heads,
+               float scale, int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  if (batch < 0 || total_q < 0) return fail(MLA_ERR_INVALID_ARG, "batch and total_q must be >= 0");
+  if (num_heads < 1 || num_heads > 1024) return fail(MLA_ERR_INVALID_ARG, "num_heads must be in [1, 1024]");
+  if (batch == 0 || total_q == 0) return ok();
+  if (!query_start_loc && total_q != batch)
+    return fail(MLA_ERR_INVALID_ARG, "without query_start_loc every request has one query token (total_q == batch)");
+  if (!q_abs || !q_pe || !cache || !block_table || !seq_lens || !out || !workspace)
+    return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_abs, 16) || !aligned(q_pe, 16) || !aligned(cache, 16) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARG, "q_abs, q_pe, cache and out must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (query_start_loc && !aligned(query_start_loc, 4)) ||
+      (lse && !aligned(lse, 4)))
+    return fail(MLA_ERR_INVALID_ARG, "block_table, seq_lens, query_start_loc and lse must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (!valid_page_size(page_size))
+    return fail(MLA_ERR_UNSUPPORTED, "page_size must be 16, 32, 64, 128 or 256 (got %d)", page_size);
+  if (num_blocks <= 0 || num_blocks * (int64_t)page_size >= (int64_t)1 << 31)
+    return fail(MLA_ERR_INVALID_ARG, "num_blocks * page_size must be in [1, 2^31)");
+  if (max_pages_per_seq <= 0) return fail(MLA_ERR_INVALID_ARG, "max_pages_per_seq must be positive");
+  if ((int64_t)total_q * num_heads >= ((int64_t)1 << 31) - 1024)
+    return fail(MLA_ERR_INVALID_ARG, "total_q * num_heads must be below 2^31");
+  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
+  if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
+  if (!std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite");
+  if (num_splits < 0 || num_splits > 4096) return fail(MLA_ERR_INVALID_ARG, "num_splits must be in [0, 4096]");
+  if (cache_dtype == MLA_FP8_E4M3) return fail(MLA_ERR_UNSUPPORTED, "fp8 cache decode is not built yet");
+
+  const mla::WorkspaceLayout L = mla::workspace_layout(batch, total_q, num_heads, num_splits);
+  if (workspace_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes, L.total);
+  const int sms = sm_count();
+  if (sms < 2) return fail(MLA_ERR_CUDA, "cannot query the current device");
+  const int clusters = sms / 2 < mla::kMaxClusters ? sms / 2 : mla::kMaxClusters;
+
+  const uint64_t rows = (uint64_t)total_q * num_heads;
+  CUtensorMap tm_q, tm_qpe, tm_kv;
+  const uint32_t kv_box_rows = page_size < 64 ? page_size : 64;
+  if (!mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !mla::encode_tmap_2d(&tm_qpe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk,
+                           (uint64_t)num_blocks * page_size, mla::kDqk * 2, 64, kv_box_rows,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
+
+  mla::DecodeArgs a{};
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.qsl = query_start_loc;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.max_pages = max_pages_per_seq;
+  a.page_size = page_size;
+  a.num_blocks = (int)num_blocks;
+  a.total_rows = (int)rows;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out_scale = 1.f;
+  a.out = out;
+  a.lse = lse;
+  a.plan = mla::plan_from_workspace(workspace, L);
+
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = mla::launch_plan(seq_lens, query_start_loc, batch, num_heads, max_pages_per_seq, page_size,
+                                   num_splits, clusters, a.plan, s);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  const bool timed = g_timing_start && g_timing_stop;
+  if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
+  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, cache_dtype, a, clusters, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
+  e = mla::launch_combine(a, L.max_groups, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return ok();
+}
+
+int mla_decode_status(const void* workspace, int* status, void* stream) {
+  if (!workspace || !status) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(status, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  return ok();
+}
+
+int mla_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, int64_t rows, int dim,
+                     int o_dtype, void* out, float* lse_out, void* stream) {
+  if (rows < 0) return fail(MLA_ERR_INVALID_ARG, "rows must be >= 0");
+  if (dim <= 0 || dim % 8 != 0 || dim > 4096) return fail(MLA_ERR_INVALID_ARG, "dim must be a multiple of 8 in [8, 4096]");
+  if (o_dtype != MLA_BF16 && o_dtype != MLA_FP32)
+    return fail(MLA_ERR_INVALID_ARG, "o_dtype must be MLA_BF16 or MLA_FP32 (got %d)", o_dtype);
+  if (rows == 0) return ok();
+  if (!o_a || !lse_a || !o_b || !lse_b || !out) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(o_a, 16) || !aligned(o_b, 16) || !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARG, "o_a, o_b and out must be 16-byte aligned");
+  if (!aligned(lse_a, 4) || !aligned(lse_b, 4) || (lse_out && !aligned(lse_out, 4)))
+    return fail(MLA_ERR_INVALID_ARG, "LSE arrays must be 4-byte aligned");
+  if (lse_out && (lse_out == lse_a || lse_out == lse_b))
+    return fail(MLA_ERR_INVALID_ARG, "lse_out must not alias lse_a or lse_b");
+  cudaError_t e = mla::launch_merge_states(o_a, lse_a, o_b, lse_b, rows, dim, o_dtype == MLA_BF16, out, lse_out,
+                                           (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return ok();
+}
+
+}  // extern "C"

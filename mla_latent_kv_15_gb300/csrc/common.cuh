@@ -1,0 +1,135 @@
+// Shared definitions of the MLA decode library: fixed widths, the split-KV
+// plan that lives in the caller's workspace, and the launchers each
+// translation unit exports to the C-ABI layer (api.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kLkv = 512;          // latent width (kv_c, q_abs, output)
+constexpr int kRope = 64;          // decoupled rope width (k_pe, q_pe)
+constexpr int kDqk = kLkv + kRope; // cache row width
+constexpr int kRows = 128;         // query rows per work unit (tcgen05 M)
+constexpr int kTile = 64;          // keys per tile (S MMA N, P.V MMA K)
+constexpr int kMaxClusters = 128;  // upper bound of CTA pairs in the decode grid
+
+// Work-unit plan written by the scheduler kernel into the workspace.
+//   group  = up to 128 consecutive query rows (flattened t*N + h) of one request
+//   unit   = a contiguous tile range of one group, processed by one CTA pair
+struct PlanHeader {
+  int status;        // OR of mla_device_error bits
+  int num_groups;
+  int num_units;
+  int num_clusters;
+  int total_tiles;
+  int tiles_per_cluster;
+  int pad[2];
+};
+
+struct GroupRec {    // 32 bytes
+  int b;             // request
+  int row0;          // first flattened query row (t*N + h)
+  int nrows;         // rows in this group (<= 128)
+  int lmax;          // keys visible to the group's last row (>= 0)
+  int pieces;        // units the group was cut into (0: no keys)
+  int ubase;         // index of its first unit
+  int tiles;         // ceil(lmax / 64)
+  int tpos;          // position of its first tile on the flattened tile axis
+};
+
+struct UnitRec {     // 16 bytes
+  int group;
+  int tile_begin;
+  int tile_end;
+  int slot;          // partial-result slot (== unit index) or -1: write the final output
+};
+
+struct Plan {
+  PlanHeader* header;
+  GroupRec* groups;
+  UnitRec* units;
+  int* unit_cluster;     // cluster index of each unit
+  int* cluster_begin;    // [kMaxClusters + 1] first unit of each cluster
+  float* part_o;         // [max_units][128][512]
+  float* part_lse;       // [max_units][128]
+  int max_groups;
+  int max_units;
+};
+
+struct WorkspaceLayout {
+  size_t header, groups, units, unit_cluster, cluster_begin, part_o, part_lse, total;
+  int max_groups, max_units;
+};
+
+// Byte offsets of each plan array for a batch shape (host and device agree).
+inline WorkspaceLayout workspace_layout(int batch, int total_q, int num_heads, int max_splits) {
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  WorkspaceLayout L{};
+  long long rows = (long long)total_q * num_heads;
+  long long mg = (rows + 127LL * batch) / kRows + 1;
+  long long mu = mg * (max_splits > 1 ? max_splits : 1) + kMaxClusters;
+  L.max_groups = (int)mg;
+  L.max_units = (int)mu;
+  size_t off = 0;
+  L.header = off;        off = up(off + sizeof(PlanHeader));
+  L.groups = off;        off = up(off + sizeof(GroupRec) * (size_t)mg);
+  L.units = off;         off = up(off + sizeof(UnitRec) * (size_t)mu);
+  L.unit_cluster = off;  off = up(off + sizeof(int) * (size_t)mu);
+  L.cluster_begin = off; off = up(off + sizeof(int) * (kMaxClusters + 1));
+  L.part_o = off;        off = up(off + sizeof(float) * (size_t)mu * kRows * kLkv);
+  L.part_lse = off;      off = up(off + sizeof(float) * (size_t)mu * kRows);
+  L.total = off;
+  return L;
+}
+
+inline Plan plan_from_workspace(void* ws, const WorkspaceLayout& L) {
+  char* p = static_cast<char*>(ws);
+  Plan P;
+  P.header = reinterpret_cast<PlanHeader*>(p + L.header);
+  P.groups = reinterpret_cast<GroupRec*>(p + L.groups);
+  P.units = reinterpret_cast<UnitRec*>(p + L.units);
+  P.unit_cluster = reinterpret_cast<int*>(p + L.unit_cluster);
+  P.cluster_begin = reinterpret_cast<int*>(p + L.cluster_begin);
+  P.part_o = reinterpret_cast<float*>(p + L.part_o);
+  P.part_lse = reinterpret_cast<float*>(p + L.part_lse);
+  P.max_groups = L.max_groups;
+  P.max_units = L.max_units;
+  return P;
+}
+
+// Everything the decode kernel needs besides its tensor maps.
+struct DecodeArgs {
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* qsl;       // may be null: one query token per request
+  int batch;
+  int num_heads;
+  int max_pages;
+  int page_size;
+  int num_blocks;
+  int total_rows;           // total_q * num_heads: bound of every output row
+  float scale_log2;         // scale * log2(e) (* kv_scale for fp8)
+  float out_scale;          // kv_scale for fp8, 1 for bf16
+  void* out;                // bf16 [T*N, 512]
+  float* lse;               // [T*N] or null
+  Plan plan;
+};
+
+// ---- launchers (return cudaError_t of the launch)
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
+                        int page_size, int num_splits, int num_clusters, Plan plan, cudaStream_t s);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
+                          int cache_dtype, const DecodeArgs& a, int num_clusters, cudaStream_t s);
+cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
+cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                                int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,
+                                cudaStream_t s);
+cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
+                               void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s);
+size_t decode_smem_bytes(int cache_dtype);
+
+}  // namespace mla

@@ -1,0 +1,208 @@
+// Split-KV scheduler: builds the work-unit plan of one mla_decode call on the
+// device (no host synchronisation, so the whole decode can be captured in a
+// CUDA graph).
+//
+// Query rows of a request are flattened as t*N + h and cut into groups of up
+// to 128 rows (the tcgen05 M of the decode kernel).  Every group reads the
+// keys its last row may see, L = seq_len - Sq + 1 + t (multi-token causal
+// rule of the AITER MLA backend's verify path), in 64-key tiles.  Groups are
+// laid end to end on one flattened tile axis which is either
+//   * cut into equal spans, one per CTA pair (automatic: every pair gets
+//     ceil(total_tiles / clusters) tiles, a group straddling a boundary is
+//     split there), or
+//   * with num_splits = k, every group is cut into min(k, tiles) near-equal
+//     pieces and pieces go to the pair whose span holds their midpoint.
+// Pieces of a split group write fp32 partials that the combine kernel merges
+// with the LSE rule of merge_attn_states.
+#include "common.cuh"
+
+namespace mla {
+
+namespace {
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// Exclusive scan over the block (blockDim.x == 1024); *total gets the sum.
+__device__ int block_excl_scan(int v, int* total) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_total;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = warp_incl_scan(v);
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+    int wi = warp_incl_scan(w);
+    warp_sums[lane] = wi - w;
+    if (lane == 31) s_total = wi;
+  }
+  __syncthreads();
+  int r = incl - v + warp_sums[warp];
+  *total = s_total;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
+                                                    const int32_t* __restrict__ qsl, int batch, int N,
+                                                    int max_pages, int page_size, int num_splits, int C,
+                                                    Plan P) {
+  __shared__ int s_flags;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_flags = 0;
+  __syncthreads();
+  const long long kv_cap = (long long)max_pages * page_size;
+
+  // 1. groups of every request
+  int carry = 0;
+  for (int base = 0; base < batch; base += 1024) {
+    const int b = base + tid;
+    int sq = 0, ng = 0;
+    if (b < batch) {
+      sq = qsl ? qsl[b + 1] - qsl[b] : 1;
+      if (sq < 0) sq = 0;
+      ng = (int)(((long long)sq * N + kRows - 1) / kRows);
+    }
+    int total;
+    const int gb = block_excl_scan(ng, &total) + carry;
+    if (b < batch && ng > 0) {
+      const int q0 = qsl ? qsl[b] : b;
+      long long seq = seq_lens[b];
+      if (seq > kv_cap) {
+        atomicOr(&s_flags, 2);  // MLA_DEVERR_BAD_SEQ_LEN
+        seq = kv_cap;
+      }
+      const int rows_b = sq * N;
+      for (int g = 0; g < ng && gb + g < P.max_groups; ++g) {
+        GroupRec r;
+        r.b = b;
+        r.row0 = q0 * N + g * kRows;
+        r.nrows = min(kRows, rows_b - g * kRows);
+        const int t_last = (g * kRows + r.nrows - 1) / N;
+        long long L = seq - sq + 1 + t_last;
+        if (L < 0) L = 0;
+        if (L > kv_cap) L = kv_cap;
+        r.lmax = (int)L;
+        r.tiles = (int)((L + kTile - 1) / kTile);
+        r.pieces = 0;
+        r.ubase = 0;
+        r.tpos = 0;
+        P.groups[gb + g] = r;
+      }
+    }
+    carry += total;
+  }
+  int G = carry;
+  if (G > P.max_groups) {  // query_start_loc disagrees with total_q: plan nothing
+    if (tid == 0) atomicOr(&s_flags, 8);  // MLA_DEVERR_BAD_QSL
+    G = 0;
+  }
+  __syncthreads();
+
+  // 2. flattened tile positions
+  carry = 0;
+  for (int base = 0; base < G; base += 1024) {
+    const int g = base + tid;
+    const int t = g < G ? P.groups[g].tiles : 0;
+    int total;
+    const int pos = block_excl_scan(t, &total) + carry;
+    if (g < G) P.groups[g].tpos = pos;
+    carry += total;
+  }
+  const int T = carry;
+  const int W = T > 0 ? (T + C - 1) / C : 1;
+  __syncthreads();
+
+  // 3. pieces per group, unit bases
+  carry = 0;
+  for (int base = 0; base < G; base += 1024) {
+    const int g = base + tid;
+    int pieces = 0;
+    if (g < G) {
+      const GroupRec r = P.groups[g];
+      if (r.tiles > 0) {
+        if (num_splits > 0)
+          pieces = min(num_splits, r.tiles);
+        else
+          pieces = (r.tpos + r.tiles - 1) / W - r.tpos / W + 1;
+      }
+    }
+    int total;
+    const int ub = block_excl_scan(pieces, &total) + carry;
+    if (g < G) {
+      P.groups[g].pieces = pieces;
+      P.groups[g].ubase = ub;
+    }
+    carry += total;
+  }
+  int U = carry;
+  if (U > P.max_units) {  // cannot happen for a workspace sized for num_splits
+    __syncthreads();
+    for (int g = tid; g < G; g += 1024) P.groups[g].pieces = 0;
+    if (tid == 0) atomicOr(&s_flags, 8);
+    U = 0;
+  }
+  __syncthreads();
+
+  // 4. units
+  for (int g = tid; g < G; g += 1024) {
+    const GroupRec r = P.groups[g];
+    for (int i = 0; i < r.pieces; ++i) {
+      UnitRec u;
+      int cl;
+      u.group = g;
+      if (num_splits > 0) {
+        u.tile_begin = (int)((long long)i * r.tiles / r.pieces);
+        u.tile_end = (int)((long long)(i + 1) * r.tiles / r.pieces);
+        cl = min(C - 1, (r.tpos + (u.tile_begin + u.tile_end) / 2) / W);
+      } else {
+        cl = r.tpos / W + i;
+        u.tile_begin = max(r.tpos, cl * W) - r.tpos;
+        u.tile_end = min(r.tpos + r.tiles, (cl + 1) * W) - r.tpos;
+      }
+      u.slot = r.pieces > 1 ? r.ubase + i : -1;
+      P.units[r.ubase + i] = u;
+      P.unit_cluster[r.ubase + i] = cl;
+    }
+  }
+  __syncthreads();
+
+  // 5. first unit of every cluster (unit clusters are non-decreasing)
+  for (int u = tid; u < U; u += 1024) {
+    const int c = P.unit_cluster[u];
+    const int cp = u > 0 ? P.unit_cluster[u - 1] : -1;
+    for (int k = cp + 1; k <= c; ++k) P.cluster_begin[k] = u;
+  }
+  if (tid == 0) {
+    const int last = U > 0 ? P.unit_cluster[U - 1] : -1;
+    for (int k = last + 1; k <= kMaxClusters; ++k) P.cluster_begin[k] = U;
+    PlanHeader h;
+    h.status = s_flags;
+    h.num_groups = G;
+    h.num_units = U;
+    h.num_clusters = C;
+    h.total_tiles = T;
+    h.tiles_per_cluster = W;
+    h.pad[0] = h.pad[1] = 0;
+    *P.header = h;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
+                        int page_size, int num_splits, int num_clusters, Plan plan, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, qsl, batch, num_heads, max_pages, page_size, num_splits,
+                                 num_clusters, plan);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -26,6 +26,7 @@ Arrays are numpy; bf16 values are carried as their uint16 bit patterns.
 from __future__ import annotations
 
 import math
+import os
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -60,6 +61,28 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     import torch
     t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _normal_bf16_pages(seed: int, npages: int, page_size: int) -> np.ndarray:
+    """N(0,1)*0.5 latent rows for `npages` pages as bf16 bits, drawn in chunks of
+    256 pages, each from its own PCG64 stream spawned from `seed` (the result
+    does not depend on how many threads draw them)."""
+    import concurrent.futures as cf
+    chunk = 256
+    n = (npages + chunk - 1) // chunk
+    seqs = np.random.SeedSequence([seed, 0x5EED]).spawn(n)
+    out = np.empty((npages, page_size, DQK), dtype=np.uint16)
+
+    def fill(i):
+        lo, hi = i * chunk, min(npages, (i + 1) * chunk)
+        g = np.random.Generator(np.random.PCG64(seqs[i]))
+        v = g.standard_normal((hi - lo, page_size, DQK), dtype=np.float32)
+        v *= np.float32(0.5)
+        out[lo:hi] = to_bf16_bits(v)
+
+    with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 4)) as ex:
+        list(ex.map(fill, range(n)))
+    return out
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -146,8 +169,7 @@ def make_decode_case(*, num_heads: int, batch: int, ctx: tuple[int, int], sq=1,
     else:
         pool[...] = 0
     if used.size:
-        vals = rng.standard_normal((used.size, page_size, DQK), dtype=np.float32) * np.float32(0.5)
-        pool[used] = to_bf16_bits(vals)
+        pool[used] = _normal_bf16_pages(seed, used.size, page_size)
     new = rng.standard_normal((total_q, DQK), dtype=np.float32) * np.float32(0.5)
     newb = to_bf16_bits(new)
 
@@ -160,15 +182,11 @@ def make_decode_case(*, num_heads: int, batch: int, ctx: tuple[int, int], sq=1,
                 slots[qsl[b] + t] = -1           # nothing to write (padding token)
             else:
                 slots[qsl[b] + t] = int(table[b, pos // page_size]) * page_size + pos % page_size
-    # every readable slot (used to prepare an fp8 cache from the bf16 pool)
-    ref = []
-    for b in range(batch):
-        n = int(lens[b])
-        if n <= 0:
-            continue
-        pos = np.arange(n, dtype=np.int64)
-        ref.append(table[b, pos // page_size].astype(np.int64) * page_size + pos % page_size)
-    ref_slots = np.concatenate(ref) if ref else np.zeros(0, dtype=np.int64)
+    # every slot of every referenced page (used to prepare an fp8 cache from
+    # the bf16 pool; whole pages, so rows past seq_len in a last page are
+    # finite values too, as a real writer leaves them)
+    ref_slots = (used.astype(np.int64)[:, None] * page_size
+                 + np.arange(page_size, dtype=np.int64)[None, :]).ravel()
 
     kv_scale = 1.0
     if cache_dtype == "fp8":

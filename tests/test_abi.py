@@ -1,0 +1,92 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_latent_kv_15_gb300 import _build
+    import mla_latent_kv_15_gb300 as mla
+    _build.build()
+    return mla.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    return re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("mla_cache_write", "mla_decode", "mla_merge_states", "mla_decode_workspace_size", "mla_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import mla_latent_kv_15_gb300 as mla
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+    assert set(declared_symbols()) == set(mla.C_ABI_SYMBOLS)
+
+
+def test_workspace_size_grows_with_splits(lib):
+    a = lib.mla_decode_workspace_size(64, 64, 128, 0)
+    b = lib.mla_decode_workspace_size(64, 64, 128, 16)
+    assert 0 < a < b
+    assert lib.mla_decode_workspace_size(0, 64, 128, 0) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)          # never dereferenced: validation fails first
+    # num_heads out of range
+    rc = lib.mla_decode(fake, fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 2, 0, 0.1, 0, fake, None,
+                        fake, 1 << 30, None)
+    assert rc == -1 and b"num_heads" in lib.mla_last_error()
+    # unsupported page size
+    rc = lib.mla_decode(fake, fake, fake, 10, 48, 0, 1.0, fake, 4, fake, 2, None, 2, 16, 0.1, 0, fake, None,
+                        fake, 1 << 30, None)
+    assert rc == -2 and b"page_size" in lib.mla_last_error()
+    # misaligned q_abs
+    rc = lib.mla_decode(P((1 << 20) + 2), fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 2, 16, 0.1, 0, fake,
+                        None, fake, 1 << 30, None)
+    assert rc == -1 and b"aligned" in lib.mla_last_error()
+    # total_q != batch without query_start_loc
+    rc = lib.mla_decode(fake, fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 3, 16, 0.1, 0, fake, None,
+                        fake, 1 << 30, None)
+    assert rc == -1
+    # workspace too small
+    rc = lib.mla_decode(fake, fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 2, 16, 0.1, 0, fake, None,
+                        P(1 << 24), 16, None)
+    assert rc == -4
+    # fp8 with a bad scale
+    rc = lib.mla_cache_write(fake, fake, fake, 4, fake, 10, 64, 1, 0.0, None)
+    assert rc == -1 and b"kv_scale" in lib.mla_last_error()
+    # merge: bad dim, aliasing LSE
+    rc = lib.mla_merge_states(fake, fake, fake, fake, 10, 12, 2, fake, None, None)
+    assert rc == -1
+    rc = lib.mla_merge_states(fake, P(64), fake, P(128), 10, 512, 2, fake, P(64), None)
+    assert rc == -1 and b"alias" in lib.mla_last_error()
+    # empty work is a no-op that never touches the device
+    assert lib.mla_decode(None, None, None, 1, 64, 0, 1.0, None, 1, None, 0, None, 0, 16, 0.1, 0, None, None,
+                          None, 0, None) == 0
+    assert lib.mla_cache_write(None, None, None, 0, None, 1, 64, 0, 1.0, None) == 0
+    assert lib.mla_last_error() == b""
+
+
+def test_product_fails_loudly_without_library(tmp_path):
+    """No fallback: a missing library is an ImportError, not a CPU path."""
+    import mla_latent_kv_15_gb300 as mla
+    saved = mla._lib
+    mla._lib = None
+    try:
+        with pytest.raises(ImportError):
+            mla.load(str(tmp_path / "missing.so"))
+    finally:
+        mla._lib = saved

@@ -1,0 +1,183 @@
+"""GPU parity of the CUDA library (through its C ABI) against the fp64 oracle.
+
+Bars: cache write and paged gather bit-exact; latent output max abs error
+<= 2e-2 (bf16 cache) or <= 6e-2 (fp8 cache, against the oracle on dequantised
+values); LSE max abs error <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import mla_latent_kv_15_gb300 as mla
+    from gpu_case import GpuCase, compare, sample_rows, bf16_tensor, LKV, DQK
+
+
+# ----------------------------------------------------------------- cache write
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_cache_write_bitexact(dtype, page_size):
+    case = synth.make_decode_case(num_heads=4, batch=37, ctx=(1, 300), sq=[1, 3] * 18 + [2], page_size=page_size,
+                                  cache_dtype=dtype, seed=31, poison=False)
+    slots = case.slot_mapping.copy()
+    slots[5] = -1                                             # a padding token
+    g = GpuCase(case, write_new=False)
+    before = g.cache.view(torch.uint8).cpu().numpy().copy()
+    mla.cache_write(g.new_kv_c, g.new_k_pe, torch.from_numpy(slots).cuda(), g.cache, case.kv_scale)
+    torch.cuda.synchronize()
+    got = g.cache.view(torch.uint8).cpu().numpy()
+    # oracle: the same write applied on the host to the same starting bytes
+    if dtype == "bf16":
+        ref = before.view(np.uint16).reshape(case.pool.shape).copy()
+        oracle.cache_write(case.new_kv_c, case.new_k_pe, slots, ref, page_size, oracle.CACHE_BF16)
+        ref = ref.view(np.uint8)
+    else:
+        ref = before.reshape(case.pool.shape).copy()
+        oracle.cache_write(case.new_kv_c, case.new_k_pe, slots, ref, page_size, oracle.CACHE_E4M3, case.kv_scale)
+    assert np.array_equal(got.reshape(-1), ref.reshape(-1))
+
+
+def test_cache_write_preparation_matches_oracle_fp8():
+    """The whole fp8 cache the decode tests read (every referenced row
+    quantised on the GPU) is bit-identical to the oracle's."""
+    case = synth.make_decode_case(num_heads=2, batch=6, ctx=(50, 400), page_size=64, cache_dtype="fp8", seed=32)
+    g = GpuCase(case)
+    torch.cuda.synchronize()
+    ref = oracle.prepare_cache(case)
+    got = g.cache.view(torch.uint8).cpu().numpy()
+    used = np.unique(case.referenced_slots // 64)
+    assert np.array_equal(got[used], ref[used])
+
+
+# ----------------------------------------------------------------------- merge
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_merge_states(dtype):
+    rows = 3000
+    o_a, lse_a, o_b, lse_b = synth.random_partials(5, rows, 512, neg_inf_frac=0.05)
+    ta, tb = torch.from_numpy(o_a).cuda().to(dtype), torch.from_numpy(o_b).cuda().to(dtype)
+    la, lb = torch.from_numpy(lse_a).cuda(), torch.from_numpy(lse_b).cuda()
+    out = torch.empty_like(ta)
+    lo = torch.empty_like(la)
+    mla.merge_states(ta, la, tb, lb, out, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.merge(ta.float().cpu().numpy(), lse_a, tb.float().cpu().numpy(), lse_b)
+    got = out.float().cpu().numpy()
+    tol = 1e-5 if dtype == torch.float32 else 1e-2
+    assert np.max(np.abs(got - ref_o)) <= tol
+    fin = np.isfinite(ref_l)
+    gl = lo.cpu().numpy()
+    assert np.array_equal(np.isfinite(gl), fin)
+    assert np.max(np.abs(gl[fin] - ref_l[fin])) <= 1e-5
+    # in place: out aliases o_a
+    mla.merge_states(ta, la, tb, lb, ta, None)
+    torch.cuda.synchronize()
+    assert torch.equal(ta, out)
+
+
+# ---------------------------------------------------------------------- decode
+
+def test_decode_tiny_config_all_rows():
+    """N=16, ctx 256, page 64, 4 of 8 pages permuted: every row vs the oracle."""
+    case = synth.workload("tiny_n16_ctx256")
+    g = GpuCase(case)
+    g.decode()
+    compare(case, g)
+    assert mla.decode_status(g.workspace) == 0
+
+
+@pytest.mark.parametrize("num_heads,sq,page_size,num_splits", [
+    (16, 1, 64, 0), (16, 1, 64, 3), (128, 1, 64, 0), (128, 1, 64, 1), (128, 1, 16, 2),
+    (128, 4, 64, 0), (16, 4, 32, 0), (16, [4, 1, 2, 1, 3, 1], 64, 0), (128, [4, 1, 1, 4, 2, 1], 64, 2),
+    (20, 2, 64, 0), (1, 1, 128, 0), (256, 1, 256, 0), (64, 3, 64, 5),
+])
+def test_decode_small_cases(num_heads, sq, page_size, num_splits):
+    """Several tiles with a ragged tail; splits, multi-token causal groups,
+    head counts that do not divide 128, every page size."""
+    batch = 6
+    case = synth.make_decode_case(num_heads=num_heads, batch=batch, ctx=(60, 700), sq=sq, page_size=page_size,
+                                  seed=100 + num_heads + page_size + num_splits)
+    g = GpuCase(case, num_splits_max=num_splits)
+    g.decode(num_splits)
+    compare(case, g)
+    assert mla.decode_status(g.workspace) == 0
+
+
+def test_decode_edge_lengths():
+    """seq_len 0 (padding request), Sq > seq_len, one-token contexts, exact
+    multiples of the tile, lengths one past a tile."""
+    lens = [0, 1, 2, 63, 64, 65, 128, 129, 1, 3]
+    sq = [1, 1, 4, 1, 2, 1, 1, 3, 1, 4]
+    case = synth.make_decode_case(num_heads=16, batch=len(lens), ctx=(1, 1), sq=sq, seq_lens=lens,
+                                  page_size=64, seed=41)
+    g = GpuCase(case)
+    g.decode()
+    compare(case, g)
+
+
+def test_one_token_context_returns_kv_c_bitexact():
+    """seq_len 1 on every physical page: out == kv_c of the page's first row
+    bit for bit (p = 1, l = 1), which also pins the paged gather."""
+    nb = 16
+    case = synth.make_decode_case(num_heads=32, batch=nb, ctx=(1, 1), page_size=64, num_blocks=nb, seed=42,
+                                  poison=False)
+    case.block_table[:, 0] = np.arange(nb, dtype=np.int32)[::-1]
+    case.slot_mapping[:] = -1                                  # keep the drawn rows
+    g = GpuCase(case)
+    g.decode()
+    got = g.out.view(torch.int16).cpu().numpy().view(np.uint16)       # [nb, 32, 512]
+    want = case.pool[case.block_table[:, 0], 0, :LKV]                 # [nb, 512]
+    assert np.array_equal(got, np.broadcast_to(want[:, None, :], got.shape))
+
+
+def test_split_counts_agree():
+    """Automatic and forced splits (1, 2, 7 pieces) give the same result within
+    the fp32 merge rounding."""
+    case = synth.make_decode_case(num_heads=128, batch=5, ctx=(500, 2000), page_size=64, seed=43)
+    g = GpuCase(case, num_splits_max=7)
+    res = []
+    for k in (0, 1, 2, 7):
+        o, l = g.decode(k)
+        res.append((o.float().clone(), l.clone()))
+        compare(case, g)
+    for o, l in res[1:]:
+        assert torch.max(torch.abs(o - res[0][0])).item() <= 1.6e-2
+        assert torch.max(torch.abs(l - res[0][1])).item() <= 1e-4
+
+
+def test_block_id_out_of_range_flags_and_does_not_fault():
+    case = synth.make_decode_case(num_heads=16, batch=2, ctx=(100, 200), page_size=64, seed=44, poison=False)
+    g = GpuCase(case)
+    bt = g.block_table.clone()
+    bt[0, 0] = case.num_blocks + 5
+    g.block_table = bt
+    g.decode()
+    assert mla.decode_status(g.workspace) & mla.DEVERR_BAD_BLOCK
+
+
+# --------------------------------------------------------- full-size workloads
+
+FULL = [("dsv3_n128_b64_ctx1k-8k", (0,)), ("n16_b128_ctx8k-32k", (0, 4, 16)),
+        ("mtp_n128_sq4_b32_ctx2k-16k", (0,)), ("mtp_mixed_n128_b32_ctx2k-16k", (0,))]
+
+
+@pytest.mark.parametrize("name,splits", FULL)
+def test_full_size_sampled_rows(name, splits):
+    """Serving-shaped batches at full size in the launch configuration the
+    benchmark uses (automatic split; forced 4 and 16 splits for the long
+    contexts); sampled rows against the oracle."""
+    case = synth.workload(name)
+    g = GpuCase(case, num_splits_max=max(splits))
+    cache_host = oracle.prepare_cache(case)
+    rows = sample_rows(case, 300, seed=7)
+    for k in splits:
+        g.out.fill_(float("nan"))
+        g.decode(k)
+        compare(case, g, rows=rows, cache_host=cache_host)
+        assert mla.decode_status(g.workspace) == 0
