@@ -186,6 +186,36 @@ MLA_API int mla_merge_states(const void* o_a, const float* lse_a, const void* o_
  */
 MLA_API int mla_set_decode_timing_events(void* start, void* stop);
 
+/*
+ * mla_decode_no_alloc -- mla_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart of this entry point; it exists for
+ * callers that are not allowed to call cudaMalloc or any other allocating
+ * routine around a decode step (for example while a CUDA graph is being
+ * captured, or in a runtime whose host framework owns every device buffer).
+ *
+ * Arguments and results are those of mla_decode without `workspace` and
+ * `workspace_bytes`: inputs and outputs still come from the caller.  The
+ * split-KV scratch is a fixed device array of MLA_NO_ALLOC_SCRATCH_BYTES
+ * (96 MiB) inside the library; every GPU that loads the library holds it until
+ * the process exits.  A batch whose scratch need
+ * (mla_decode_workspace_size(batch, total_q, num_heads, num_splits)) exceeds
+ * it is rejected with MLA_ERR_WORKSPACE before anything is enqueued.  The
+ * first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  No call
+ * allocates memory.
+ *
+ * All calls share the one array and it keeps the last call's contents, so
+ * calls that may overlap on the GPU (different streams, different host
+ * threads) race: serialise them on one stream.  The device error word of
+ * these calls lives in the shared array and is not exposed.
+ */
+#define MLA_NO_ALLOC_SCRATCH_BYTES ((size_t)96 << 20)
+MLA_API int mla_decode_no_alloc(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks,
+                                int page_size, int cache_dtype, float kv_scale, const int32_t* block_table,
+                                int max_pages_per_seq, const int32_t* seq_lens, int batch,
+                                const int32_t* query_start_loc, int total_q, int num_heads, float scale,
+                                int num_splits, void* out, float* lse, void* stream);
+
 /* Human-readable description of the calling thread's last error ("" if none). */
 MLA_API const char* mla_last_error(void);
 

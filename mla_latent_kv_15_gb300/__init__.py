@@ -27,7 +27,9 @@ ROPE = 64
 DQK = 576
 
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
-                 "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events")
+                 "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
+                 "mla_decode_no_alloc")
+NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
 
@@ -63,6 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_device_sm_count.argtypes = []
     lib.mla_set_decode_timing_events.restype = i32
     lib.mla_set_decode_timing_events.argtypes = [P, P]
+    lib.mla_decode_no_alloc.restype = i32
+    lib.mla_decode_no_alloc.argtypes = [P, P, P, i64, i32, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P]
     _lib = lib
     return lib
 
@@ -114,6 +118,20 @@ def decode(q_abs, q_pe, cache, block_table, seq_lens, out, workspace, *, scale: 
                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
                              T, N, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_no_alloc(q_abs, q_pe, cache, block_table, seq_lens, out, *, scale: float, query_start_loc=None,
+                    lse=None, num_splits: int = 0, kv_scale: float = 1.0, stream=None) -> None:
+    """decode() for callers that cannot allocate: the split-KV scratch is the
+    library's own fixed 96 MiB device array (shared by all calls; calls that
+    overlap on the GPU race).  Batches needing more scratch raise MLAError."""
+    T, N, _ = q_abs.shape
+    nb, ps, _ = cache.shape
+    B = seq_lens.numel()
+    _check(load().mla_decode_no_alloc(_ptr(q_abs), _ptr(q_pe), _ptr(cache), nb, ps, _dtype_code(cache),
+                                      float(kv_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                      _ptr(query_start_loc), T, N, float(scale), int(num_splits), _ptr(out),
+                                      _ptr(lse), _stream(stream)))
 
 
 def decode_status(workspace, stream=None) -> int:

@@ -49,6 +49,12 @@ bool valid_page_size(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps == 
 
 }  // namespace
 
+namespace mla {
+// Lets entry points defined in other translation units report an error
+// through mla_last_error().
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
