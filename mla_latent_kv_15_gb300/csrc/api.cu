@@ -138,7 +138,7 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
 
   const uint64_t rows = (uint64_t)total_q * num_heads;
   CUtensorMap tm_q, tm_qpe, tm_kv;
-  const uint32_t kv_box_rows = page_size < 64 ? page_size : 64;
+  const uint32_t kv_box_rows = page_size < mla::kTile ? page_size : mla::kTile;
   if (!mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64, 64,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !mla::encode_tmap_2d(&tm_qpe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 64, 64,

@@ -37,7 +37,7 @@ struct GroupRec {    // 32 bytes
   int lmax;          // keys visible to the group's last row (>= 0)
   int pieces;        // units the group was cut into (0: no keys)
   int ubase;         // index of its first unit
-  int tiles;         // ceil(lmax / 64)
+  int tiles;         // ceil(lmax / kTile)
   int tpos;          // position of its first tile on the flattened tile axis
 };
 

@@ -1,5 +1,6 @@
 // Absorbed MLA decode on sm_103a: tcgen05 tensor cores, TMEM accumulators,
-// TMA page gathers, and a CTA pair that splits the latent width.
+// TMA page gathers, and a CTA pair that splits the 576-wide contraction of the
+// scores and the 512-wide output.
 //
 // Math (vllm/v1/attention/backends/mla/common.py, module docstring,
 // "Data-Movement Friendly Approach"): for every query row (token t, head h)
@@ -8,32 +9,35 @@
 // MLA backend: L = seq_len - Sq + 1 + t).
 //
 // Design (one work unit = <=128 query rows of one request x a tile range):
-//  * All query rows of a unit form the M = 128 dimension of both MMAs
-//      S = Q . K^T   (M=128 rows, N=64 keys,  K=576)
-//      O += P . V    (M=128 rows, N=dims,     K=64 keys),   V = kv_c.
-//  * O for 128 rows x 512 dims in fp32 would fill all of TMEM, so a CLUSTER
-//    OF TWO CTAs splits the latent width: CTA r owns output dims
-//    [256r, 256r+256) and the matching slice of the score contraction
-//    (CTA0: kv_c[0:256]; CTA1: kv_c[256:512] + k_pe).  Each CTA TMA-loads only
-//    its own columns of every cached row, so every cache byte is read from
-//    HBM once.  The two partial score tiles are exchanged through
-//    distributed shared memory (st.async with mbarrier transaction counts)
-//    and summed; both CTAs then run the identical online softmax.
-//  * TMEM (512 columns): O half [0,256), Q slice as the A operand of the score
-//    MMA [256,416), S [416,480), P (bf16, A operand of P.V) [480,512).
-//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+TMEM owner),
-//    warps 2-5 softmax / exchange / O rescale / epilogue (one query row per
-//    thread, the row's TMEM lane).
+//  * The query rows of a unit form the M = 128 dimension of every MMA.
+//  * A cluster of two CTAs shares each 64-key tile.  CTA r owns
+//      - half of the score contraction, dims [288r, 288r+288): it loads only
+//        those columns of the cached rows (plus the 64-dim box they straddle)
+//        and keeps its 288 query dims in TMEM as the A operand;
+//      - half of the output, dims [256r, 256r+256) of O += P . V.
+//    Each CTA computes a partial score tile S_r (18 MMAs, N = 64 keys), sends
+//    it to the peer as fp16 with one bulk shared-memory copy over the cluster
+//    network, and adds the peer's partial to its own (fp32) partial.  Nothing
+//    is computed twice and every cached byte is read from HBM once.
+//  * The exchange of tile i+1 is issued before tile i is processed, so the
+//    network transfer overlaps the softmax of the previous tile.
+//  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
+//    bf16 P (A operand of P.V) [464,496).
+//  * Warp roles: warp 0 TMA producer; warp 1 score-MMA issuer (+TMEM owner);
+//    warp 2 P.V-MMA issuer; warps 3-6 softmax / exchange / O rescale /
+//    epilogue (one query row per thread, the row's TMEM lane).  Two issuer
+//    warps, because one thread issues at most one MMA per ~48 cycles.
 //  * Online softmax in the exp2 domain with lazy rescaling: O and l are
 //    rescaled only when a row's running max grows by more than 8 (log2
 //    units); the final o = O / l and lse = (m + log2 l) ln 2 are exact for
-//    any reference m.
+//    any reference m.  CTA 0 writes the LSE.
 //  * Split units write fp32 partials (normalised o and lse) that the combine
 //    kernel merges (merge_attn_states rule).
 //  * Every mbarrier wait is bounded (1 s); on expiry the CTA raises its abort
 //    flag and the error word, skips all further waits and runs to the end
 //    without touching memory outside its buffers.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -43,34 +47,40 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kStages = 4;                       // cache-tile ring depth
-constexpr int kBoxBytes = 64 * 128;              // 64 rows x 64 bf16 (128 B, swizzled)
-constexpr int kStageBytes = 5 * kBoxBytes;       // up to 5 column boxes per CTA
-constexpr int kXBytes = kRows * kTile * 4;       // one partial score tile (fp32)
-constexpr int kNumThreads = 192;
+constexpr int kStages = 4;                        // ring depth (query items and cache tiles)
+constexpr int kBox = 64 * 128;                    // 64 rows x 64 bf16 (128 B rows, 128-B swizzle)
+constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 column boxes
+constexpr int kStageBytes = kBoxesPerStage * kBox;
+constexpr int kXBytes = kRows * kTile * 2;        // one fp16 partial score tile
+constexpr int kNumThreads = 224;
+constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
 
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemQ = 256;
-constexpr uint32_t kTmemS = 416;
-constexpr uint32_t kTmemP = 480;
-constexpr float kRescaleThreshold = 8.0f;        // log2 units
+constexpr uint32_t kTmemS = kTmemQ + kQCols;      // 400
+constexpr uint32_t kTmemP = kTmemS + kTile;       // 464
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
+
+static_assert(kTmemP + kTile / 2 <= 512, "TMEM columns");
 
 struct __align__(8) Barriers {
   uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t kv_empty[kStages];   // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
   uint64_t q_ready;
   uint64_t s_full;
   uint64_t s_free;
   uint64_t p_full;
-  uint64_t o_done;
-  uint64_t x_full[2];
-  uint64_t x_free[2];
-  uint64_t mma_drain;
+  uint64_t p_free;
+  uint64_t o_full;
+  uint64_t x_full[2];           // peer's partial scores landed (transaction count)
+  uint64_t x_free[2];           // the peer has consumed what we sent into its buffer
+  uint64_t s_drain;
+  uint64_t p_drain;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 2 * kXBytes + sizeof(Barriers);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 4 * (size_t)kXBytes + sizeof(Barriers);
 
 struct Ctx {
   Barriers* bars;
@@ -82,7 +92,7 @@ __device__ __forceinline__ void raise_error(const Ctx& c, int bit) {
   atomicOr(c.status, bit);
 }
 
-// Bounded wait; once the CTA has aborted every wait returns at once.
+// Bounded waits; once the CTA has aborted every wait returns at once.
 __device__ __forceinline__ void wait_bar(const Ctx& c, uint64_t* bar, uint32_t parity) {
   if (*(volatile int*)&c.bars->abort) return;
   if (!mbar_wait(smem_u32(bar), parity)) raise_error(c, 1);
@@ -102,10 +112,32 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+// Score-contraction K steps of CTA `rank`: 18 steps of 16 dims over its 288
+// dims, as (box position in the stage, 16-dim step inside the box).
+// rank 0: boxes 0-3 (all 4 steps) + box 4 steps 0,1 (dims 256-287)
+// rank 1: box 0 steps 2,3 (dims 288-319) + boxes 1-4 (all 4 steps)
+__device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
+  return rank == 0 ? (p < 4 || k < 2) : (p > 0 || k >= 2);
 }
 
 template <int kCacheFp8>
@@ -115,32 +147,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
-  uint8_t* xbuf = smem + kStages * kStageBytes;
-  Barriers* bars = reinterpret_cast<Barriers*>(xbuf + 2 * kXBytes);
+  uint8_t* x_send = stages + kStages * kStageBytes;      // 2 buffers
+  uint8_t* x_recv = x_send + 2 * kXBytes;                 // 2 buffers
+  Barriers* bars = reinterpret_cast<Barriers*>(x_recv + 2 * kXBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int cluster = (int)cluster_id_x();
-  const int nkb = rank == 0 ? 4 : 5;               // column boxes of this CTA
   const Plan& P = a.plan;
   Ctx ctx{bars, &P.header->status};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&bars->kv_full[i]), 1);
-      mbar_init(smem_u32(&bars->kv_empty[i]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[i]), 2);
     }
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), 4);
     mbar_init(smem_u32(&bars->p_full), 4);
-    mbar_init(smem_u32(&bars->o_done), 1);
+    mbar_init(smem_u32(&bars->p_free), 1);
+    mbar_init(smem_u32(&bars->o_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->x_full[i]), 1);
-      mbar_init(smem_u32(&bars->x_free[i]), 4);
+      mbar_init(smem_u32(&bars->x_free[i]), 1);
     }
-    mbar_init(smem_u32(&bars->mma_drain), 1);
+    mbar_init(smem_u32(&bars->s_drain), 1);
+    mbar_init(smem_u32(&bars->p_drain), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -171,15 +205,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       for (int u = ubeg; u < uend; ++u) {
         const UnitRec ur = P.units[u];
         const GroupRec gr = P.groups[ur.group];
+        // the CTA's 288 query dims (5 boxes of 64) for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
           const uint32_t slot = item % kStages, round = item / kStages;
           wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
           const uint32_t full = smem_u32(&bars->kv_full[slot]);
-          mbar_expect_tx(full, nkb * kBoxBytes);
+          mbar_expect_tx(full, kStageBytes);
           const int y = gr.row0 + 64 * half;
-          for (int i = 0; i < 4; ++i) tma_load_2d(st + i * kBoxBytes, &tm_q, 256 * rank + 64 * i, y, full);
-          if (rank == 1) tma_load_2d(st + 4 * kBoxBytes, &tm_qpe, 0, y, full);
+          for (int p = 0; p < kBoxesPerStage; ++p) {
+            if (rank == 1 && p == 4)
+              tma_load_2d(st + p * kBox, &tm_qpe, 0, y, full);
+            else
+              tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
+          }
         }
         const int32_t* bt = a.block_table + (size_t)gr.b * a.max_pages;
         for (int j = ur.tile_begin; j < ur.tile_end; ++j, ++item) {
@@ -187,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
           wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
           const uint32_t full = smem_u32(&bars->kv_full[slot]);
-          mbar_expect_tx(full, nkb * kBoxBytes);
+          mbar_expect_tx(full, kStageBytes);
           for (int sb = 0; sb < nsub; ++sb) {
             const int key = j * kTile + sb * sub_rows;
             const int lp = key / a.page_size;
@@ -200,93 +239,159 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 atomicOr(ctx.status, 4);
             }
             const uint32_t dst = st + sb * sub_rows * 128;
-            for (int i = 0; i < nkb; ++i) {
-              const int x = rank == 0 ? 64 * i : (i < 4 ? 256 + 64 * i : 512);
-              tma_load_2d(dst + i * kBoxBytes, &tm_kv, x, y, full);
-            }
+            for (int p = 0; p < kBoxesPerStage; ++p) tma_load_2d(dst + p * kBox, &tm_kv, 256 * rank + 64 * p, y, full);
           }
         }
       }
       // drain: every issued load has landed before the CTA may exit
       const uint32_t first = item > kStages ? item - kStages : 0;
-      for (uint32_t k = first; k < item; ++k) {
-        if (*(volatile int*)&bars->abort) {
-          // bounded even after an abort: the loads still target our own buffers
-          mbar_wait(smem_u32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
-        } else {
-          wait_bar(ctx, &bars->kv_full[k % kStages], (k / kStages) & 1);
-        }
-      }
+      for (uint32_t k = first; k < item; ++k) mbar_wait(smem_u32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------- score-MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(128, kTile, 0, 0);   // K-major keys
-      const uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);    // MN-major values
+      constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, 0, 0);   // K-major keys, N = 64
+      const uint64_t kv_desc0 = smem_desc(smem_u32(stages), 16, 1024, kSwizzle128B);
+      constexpr uint64_t kStageDesc = kStageBytes >> 4;
+      const uint32_t d = tbase + kTmemS;
+      const uint32_t qa = tbase + kTmemQ - 16 * rank;     // column of (box p, step k) = p*32 + k*8 - 16*rank
       uint32_t item = 0, it = 0, units_done = 0;
-      for (int u = ubeg; u < uend; ++u) {
+      for (int u = ubeg; u < uend; ++u, ++units_done) {
         const UnitRec ur = P.units[u];
         const int ntiles = ur.tile_end - ur.tile_begin;
-        item += 2;  // the two Q items are consumed by the softmax warps
+        item += 2;  // query items are consumed by the softmax warps
         wait_bar(ctx, &bars->q_ready, units_done & 1);
-        tc_fence_after();
-        uint32_t prev_slot = 0;
         for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
           const uint32_t slot = item % kStages, round = item / kStages;
           wait_bar(ctx, &bars->kv_full[slot], round & 1);
           wait_bar(ctx, &bars->s_free, (it & 1) ^ 1);
           tc_fence_after();
-          const uint32_t st = smem_u32(stages + slot * kStageBytes);
-          for (int i = 0; i < nkb; ++i)
+          const uint64_t kd = kv_desc0 + slot * kStageDesc;
+          bool first = true;
+#pragma unroll
+          for (int p = 0; p < kBoxesPerStage; ++p)
+#pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_ts(tbase + kTmemS, tbase + kTmemQ + i * 32 + k * 8,
-                     smem_desc(st + i * kBoxBytes + k * 32, 16, 1024, kSwizzle128B), id_s, (i | k) != 0);
+              if (kstep_valid(rank, p, k)) {
+                mma_ts(d, qa + p * 32 + k * 8, kd + ((p * kBox + k * 32) >> 4), id_s, first ? 0u : 1u);
+                first = false;
+              }
           mma_commit(smem_u32(&bars->s_full));
-          if (jj > 0) {
-            wait_bar(ctx, &bars->p_full, (it - 1) & 1);
-            tc_fence_after();
-            const uint32_t pst = smem_u32(stages + prev_slot * kStageBytes);
-            for (int k = 0; k < 4; ++k)
-              mma_ts(tbase + kTmemO, tbase + kTmemP + k * 8,
-                     smem_desc(pst + k * 2048, kBoxBytes, 1024, kSwizzle128B), id_pv, (jj > 1) || (k > 0));
-            mma_commit(smem_u32(&bars->o_done));
-            mma_commit(smem_u32(&bars->kv_empty[prev_slot]));
-          }
-          prev_slot = slot;
+          mma_commit(smem_u32(&bars->kv_empty[slot]));
         }
-        if (ntiles > 0) {
-          wait_bar(ctx, &bars->p_full, (it - 1) & 1);
-          tc_fence_after();
-          const uint32_t pst = smem_u32(stages + prev_slot * kStageBytes);
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tbase + kTmemO, tbase + kTmemP + k * 8, smem_desc(pst + k * 2048, kBoxBytes, 1024, kSwizzle128B),
-                   id_pv, (ntiles > 1) || (k > 0));
-          mma_commit(smem_u32(&bars->o_done));
-          mma_commit(smem_u32(&bars->kv_empty[prev_slot]));
-        }
-        ++units_done;
       }
-      // every issued MMA has completed before TMEM is released
-      mma_commit(smem_u32(&bars->mma_drain));
-      mbar_wait(smem_u32(&bars->mma_drain), 0);
+      mma_commit(smem_u32(&bars->s_drain));
+      mbar_wait(smem_u32(&bars->s_drain), 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------ P.V-MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);    // MN-major values, N = 256
+      // values = the CTA's output dims = boxes 0-3 of its stage; 16-key steps are 2048 B apart
+      const uint64_t v_desc0 = smem_desc(smem_u32(stages), kBox, 1024, kSwizzle128B);
+      constexpr uint64_t kStageDesc = kStageBytes >> 4;
+      uint32_t item = 0, it = 0;
+      for (int u = ubeg; u < uend; ++u) {
+        const UnitRec ur = P.units[u];
+        const int ntiles = ur.tile_end - ur.tile_begin;
+        item += 2;
+        for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
+          const uint32_t slot = item % kStages, round = item / kStages;
+          wait_bar(ctx, &bars->kv_full[slot], round & 1);
+          wait_bar(ctx, &bars->p_full, it & 1);
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + slot * kStageDesc;
+          const uint32_t pa = tbase + kTmemP;
+          mma_ts(tbase + kTmemO, pa, vd, id_pv, jj > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 1; k < kTile / 16; ++k) mma_ts(tbase + kTmemO, pa + 8 * k, vd + ((k * 2048) >> 4), id_pv, 1);
+          mma_commit(smem_u32(&bars->p_free));
+          mma_commit(smem_u32(&bars->kv_empty[slot]));
+        }
+        mma_commit(smem_u32(&bars->o_full));
+      }
+      mma_commit(smem_u32(&bars->p_drain));
+      mbar_wait(smem_u32(&bars->p_drain), 0);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------- softmax / exchange / epilogue
+    // ------------------------------------- softmax / exchange / rescale / epilogue
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q4 * 32 + lane;          // query row of this thread in the unit
     const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
-    const int tid128 = threadIdx.x - 64;
-    const uint32_t x_local[2] = {smem_u32(xbuf), smem_u32(xbuf + kXBytes)};
-    const uint32_t x_remote[2] = {mapa(x_local[0], peer), mapa(x_local[1], peer)};
-    const uint32_t xfull_remote[2] = {mapa(smem_u32(&bars->x_full[0]), peer), mapa(smem_u32(&bars->x_full[1]), peer)};
-    const uint32_t xfree_remote[2] = {mapa(smem_u32(&bars->x_free[0]), peer), mapa(smem_u32(&bars->x_free[1]), peer)};
-    const uint32_t xrow_off = (uint32_t)row * (kTile * 4);
+    const int tid128 = threadIdx.x - 96;
+    const uint32_t xrow = (uint32_t)row * (kTile * 2);
+    const uint32_t xsend0 = smem_u32(x_send), xrecv0 = smem_u32(x_recv);
+    const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
+    const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
+    const uint32_t xfree_peer0 = mapa(smem_u32(&bars->x_free[0]), peer);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
 
-    uint32_t item = 0, it = 0, od = 0;
-    for (int u = ubeg; u < uend; ++u) {
+    // Load partial scores of tile `t` from TMEM into `dst` and free the S columns.
+    auto load_s = [&](uint32_t t, float (&dst)[kTile]) {
+      wait_bar(ctx, &bars->s_full, t & 1);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tl + kTmemS, r0);
+      tmem_ld32(tl + kTmemS + 32, r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        dst[c] = __uint_as_float(r0[c]);
+        dst[32 + c] = __uint_as_float(r1[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
+    };
+    // Send partial scores of tile `t` (fp16, valid rows only) to the peer.
+    auto send_s = [&](uint32_t t, const float (&src)[kTile], uint32_t nbytes) {
+      const uint32_t b = t & 1, use = t >> 1;
+      if (tid128 == 0) bulk_wait_group_read<1>();    // the copy of tile t-2 no longer reads buffer b
+      named_bar_softmax();
+      const uint32_t base = xsend0 + b * kXBytes + xrow;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        sts128(base + ((c ^ (row & 7)) << 4), pack_f16x2(src[8 * c], src[8 * c + 1]),
+               pack_f16x2(src[8 * c + 2], src[8 * c + 3]), pack_f16x2(src[8 * c + 4], src[8 * c + 5]),
+               pack_f16x2(src[8 * c + 6], src[8 * c + 7]));
+      fence_proxy_async_smem();
+      named_bar_softmax();
+      if (tid128 == 0) {
+        wait_bar_cluster(ctx, &bars->x_free[b], (use & 1) ^ 1);
+        bulk_copy_to_peer(xrecv_peer0 + b * kXBytes, xsend0 + b * kXBytes, nbytes, xfull_peer0 + b * 8);
+        bulk_commit_group();
+      }
+    };
+    // Add the peer's partial scores of tile `t` into `acc`.
+    auto recv_s = [&](uint32_t t, float (&acc)[kTile], uint32_t nbytes) {
+      const uint32_t b = t & 1, use = t >> 1;
+      if (tid128 == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
+      wait_bar_cluster(ctx, &bars->x_full[b], use & 1);
+      __syncwarp();
+      const uint32_t base = xrecv0 + b * kXBytes + xrow;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = lds128(base + ((c ^ (row & 7)) << 4));
+        const float2 f0 = unpack_f16x2(v.x), f1 = unpack_f16x2(v.y), f2 = unpack_f16x2(v.z), f3 = unpack_f16x2(v.w);
+        acc[8 * c + 0] += f0.x;
+        acc[8 * c + 1] += f0.y;
+        acc[8 * c + 2] += f1.x;
+        acc[8 * c + 3] += f1.y;
+        acc[8 * c + 4] += f2.x;
+        acc[8 * c + 5] += f2.y;
+        acc[8 * c + 6] += f3.x;
+        acc[8 * c + 7] += f3.y;
+      }
+      named_bar_softmax();
+      if (tid128 == 0) mbar_arrive_remote(xfree_peer0 + b * 8);
+    };
+
+    uint32_t item = 0, it = 0, units_done = 0;
+    for (int u = ubeg; u < uend; ++u, ++units_done) {
       const UnitRec ur = P.units[u];
       const GroupRec gr = P.groups[ur.group];
       const int b = gr.b;
@@ -300,33 +405,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         Lr = a.seq_lens[b] - sq + 1 + tloc;
         Lr = Lr < 0 ? 0 : (Lr > gr.lmax ? gr.lmax : Lr);
       }
+      // the warp needs masking only on tiles that reach past its shortest row
+      const int lmin_warp = __reduce_min_sync(0xffffffffu, Lr);
+      const uint32_t nbytes = (uint32_t)gr.nrows * (kTile * 2);
 
-      // Q slice -> TMEM (A operand of the score MMA)
+      // the CTA's 288 query dims -> TMEM (A operand of the score MMAs)
       {
         const uint32_t my = item + (row >= 64 ? 1 : 0);
-        const uint32_t slot = my % kStages, round = my / kStages;
-        wait_bar(ctx, &bars->kv_full[slot], round & 1);
+        wait_bar(ctx, &bars->kv_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
         const int k = row & 63;
-        const uint32_t base = smem_u32(stages + slot * kStageBytes) + k * 128;
-        for (int i = 0; i < nkb; ++i) {
+        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + k * 128;
+#pragma unroll
+        for (int p = 0; p < kBoxesPerStage; ++p) {
           uint32_t q[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 v = lds128(base + i * kBoxBytes + ((c ^ (k & 7)) << 4));
+            const uint4 v = lds128(base + p * kBox + ((c ^ (k & 7)) << 4));
             q[4 * c + 0] = v.x;
             q[4 * c + 1] = v.y;
             q[4 * c + 2] = v.z;
             q[4 * c + 3] = v.w;
           }
-          tmem_st32(tl + kTmemQ + i * 32, q);
+          if (rank == 0 && p == 4) {
+            uint32_t h[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) h[c] = q[c];                    // dims 256-287
+            tmem_st16(tl + kTmemQ + 128, h);
+          } else if (rank == 1 && p == 0) {
+            uint32_t h[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) h[c] = q[16 + c];               // dims 288-319
+            tmem_st16(tl + kTmemQ, h);
+          } else {
+            tmem_st32(tl + kTmemQ + p * 32 - 16 * rank, q);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
         named_bar_softmax();
         if (tid128 == 0) {
-          mbar_arrive(smem_u32(&bars->kv_empty[item % kStages]));
-          mbar_arrive(smem_u32(&bars->kv_empty[(item + 1) % kStages]));
+          for (int qi = 0; qi < 2; ++qi) {      // two arrivals: the slot's count covers both issuers
+            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+          }
           mbar_arrive(smem_u32(&bars->q_ready));
         }
         item += 2;
@@ -334,58 +456,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 
       float m = -INFINITY, l = 0.f;
       const int ntiles = ur.tile_end - ur.tile_begin;
+      float cur[kTile], nxt[kTile];
+      if (ntiles > 0) {
+        load_s(it, cur);
+        send_s(it, cur, nbytes);
+      }
       for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
+        // exchange of the next tile first: the network copy overlaps this tile's work
+        if (jj + 1 < ntiles) {
+          load_s(it + 1, nxt);
+          send_s(it + 1, nxt, nbytes);
+        }
+        recv_s(it, cur, nbytes);
+
+        // scale (and mask on ragged tiles), tree max
         const int key0 = (ur.tile_begin + jj) * kTile;
-        float s[kTile];
-        wait_bar(ctx, &bars->s_full, it & 1);
-        __syncwarp();
-        tc_fence_after();
-        {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tl + kTmemS, r0);
-          tmem_ld32(tl + kTmemS + 32, r1);
-          tmem_wait_ld();
+        if (key0 + kTile > lmin_warp) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] = __uint_as_float(r0[c]);
-            s[32 + c] = __uint_as_float(r1[c]);
-          }
+          for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] * a.scale_log2 : -INFINITY;
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) cur[c] *= a.scale_log2;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
-
-        // exchange partial scores with the peer CTA
-        const int xb = it & 1;
-        const uint32_t xu = it >> 1;
-        wait_bar_cluster(ctx, &bars->x_free[xb], (xu & 1) ^ 1);
+        float mx[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          st_async_v4(x_remote[xb] + xrow_off + ((c ^ (row & 15)) << 4), __float_as_uint(s[4 * c]),
-                      __float_as_uint(s[4 * c + 1]), __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]),
-                      xfull_remote[xb]);
-        if (tid128 == 0) mbar_expect_tx(smem_u32(&bars->x_full[xb]), kXBytes);
-        wait_bar_cluster(ctx, &bars->x_full[xb], xu & 1);
-        __syncwarp();
+        for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(cur[c], cur[c + 16]), fmaxf(cur[c + 32], cur[c + 48]));
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 v = lds128(x_local[xb] + xrow_off + ((c ^ (row & 15)) << 4));
-          s[4 * c + 0] += __uint_as_float(v.x);
-          s[4 * c + 1] += __uint_as_float(v.y);
-          s[4 * c + 2] += __uint_as_float(v.z);
-          s[4 * c + 3] += __uint_as_float(v.w);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(xfree_remote[xb]);
-
-        // online softmax (exp2 domain)
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
-          const float v = (key0 + c < Lr) ? s[c] * a.scale_log2 : -INFINITY;
-          s[c] = v;
-          tmax = fmaxf(tmax, v);
-        }
+        for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(mx[c], mx[c + 4]), fmaxf(mx[c + 8], mx[c + 12]));
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         float alpha = 1.f;
         if (tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
@@ -393,28 +491,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
           m = tmax;
         }
         const float mref = m == -INFINITY ? 0.f : m;
-        uint32_t pk[32];
+        uint32_t pk[kTile / 2];
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = fast_exp2(s[2 * c] - mref);
-          const float p1 = fast_exp2(s[2 * c + 1] - mref);
-          l += p0 + p1;
+        for (int c = 0; c < kTile / 2; ++c) {
+          const float p0 = fast_exp2(cur[2 * c] - mref);
+          const float p1 = fast_exp2(cur[2 * c + 1] - mref);
+          ls[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }
-        if (jj > 0) {
-          wait_bar(ctx, &bars->o_done, od & 1);
-          ++od;
-          __syncwarp();
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            for (int ch = 0; ch < 8; ++ch) {
-              uint32_t o[32];
-              tmem_ld32(tl + kTmemO + ch * 32, o);
-              tmem_wait_ld();
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+
+        // P and O may be touched once the P.V of the previous tile has completed
+        wait_bar(ctx, &bars->p_free, (it & 1) ^ 1);
+        __syncwarp();
+        tc_fence_after();
+        if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t o[32];
+            tmem_ld32(tl + kTmemO + ch * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-              tmem_st32(tl + kTmemO + ch * 32, o);
-            }
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(tl + kTmemO + ch * 32, o);
           }
         }
         tmem_st32(tl + kTmemP, pk);
@@ -422,13 +521,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) cur[c] = nxt[c];
       }
 
       // epilogue
-      if (ntiles > 0) {
-        wait_bar(ctx, &bars->o_done, od & 1);
-        ++od;
-      }
+      wait_bar(ctx, &bars->o_full, units_done & 1);
       __syncwarp();
       tc_fence_after();
       const float inv = l > 0.f ? a.out_scale / l : 0.f;
@@ -467,6 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       }
       tc_fence_before();
     }
+    if (tid128 == 0) bulk_wait_group_read<0>();
   }
 
   __syncthreads();

@@ -15,49 +15,51 @@
 namespace mla {
 namespace {
 
+// Grid (groups, 32): block (g, y) merges rows 4y..4y+3 of group g, 64
+// threads per row, 8 dims per thread.
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
   const Plan& P = a.plan;
   const int g = blockIdx.x;
   if (g >= P.header->num_groups) return;
   const GroupRec gr = P.groups[g];
   if (gr.pieces == 1) return;  // written directly by the decode kernel
+  const int r = blockIdx.y * 4 + (threadIdx.x >> 6);
+  if (r >= gr.nrows) return;
+  const int R = gr.row0 + r;
+  if (R >= a.total_rows) return;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
   const int sub = threadIdx.x & 63;        // 8 dims per thread
   const int d0 = sub * 8;
-  for (int r = threadIdx.x >> 6; r < gr.nrows; r += 4) {
-    const int R = gr.row0 + r;
-    if (R >= a.total_rows) break;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float lse = -INFINITY;
-    if (gr.pieces > 1) {
-      float mx = -INFINITY;
-      for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
-      if (mx != -INFINITY) {
-        float wsum = 0.f;
-        for (int i = 0; i < gr.pieces; ++i) {
-          const size_t slot = (size_t)(gr.ubase + i);
-          const float w = __expf(P.part_lse[slot * kRows + r] - mx);
-          wsum += w;
-          const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
-          const float4 x0 = src[0], x1 = src[1];
-          acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-          acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
-        }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] *= inv;
-        lse = mx + __logf(wsum);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float lse = -INFINITY;
+  if (gr.pieces > 1) {
+    float mx = -INFINITY;
+    for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
+    if (mx != -INFINITY) {
+      float wsum = 0.f;
+      for (int i = 0; i < gr.pieces; ++i) {
+        const size_t slot = (size_t)(gr.ubase + i);
+        const float w = __expf(P.part_lse[slot * kRows + r] - mx);
+        wsum += w;
+        const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
+        const float4 x0 = src[0], x1 = src[1];
+        acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+        acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
       }
+      const float inv = 1.f / wsum;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] *= inv;
+      lse = mx + __logf(wsum);
     }
-    uint4 v;
-    __nv_bfloat162 h;
-    h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[2], acc[3]); v.y = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[4], acc[5]); v.z = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
-    *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
-    if (a.lse && sub == 0) a.lse[R] = lse;
   }
+  uint4 v;
+  __nv_bfloat162 h;
+  h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(acc[2], acc[3]); v.y = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(acc[4], acc[5]); v.z = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
+  *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
+  if (a.lse && sub == 0) a.lse[R] = lse;
 }
 
 template <bool kBf16>
@@ -144,7 +146,7 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s) {
-  combine_kernel<<<max_groups, 256, 0, s>>>(a);
+  combine_kernel<<<dim3(max_groups, kRows / 4), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
