@@ -127,7 +127,6 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
     return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
   if (!std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite");
   if (num_splits < 0 || num_splits > 4096) return fail(MLA_ERR_INVALID_ARG, "num_splits must be in [0, 4096]");
-  if (cache_dtype == MLA_FP8_E4M3) return fail(MLA_ERR_UNSUPPORTED, "fp8 cache decode is not built yet");
 
   const mla::WorkspaceLayout L = mla::workspace_layout(batch, total_q, num_heads, num_splits);
   if (workspace_bytes < L.total)
@@ -143,9 +142,13 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !mla::encode_tmap_2d(&tm_qpe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 64, 64,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk,
-                           (uint64_t)num_blocks * page_size, mla::kDqk * 2, 64, kv_box_rows,
-                           CU_TENSOR_MAP_SWIZZLE_128B))
+      !(cache_dtype == MLA_BF16
+            ? mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk,
+                                  (uint64_t)num_blocks * page_size, mla::kDqk * 2, 64, kv_box_rows,
+                                  CU_TENSOR_MAP_SWIZZLE_128B)
+            : mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk,
+                                  (uint64_t)num_blocks * page_size, mla::kDqk, 64, kv_box_rows,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE)))
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
 
   mla::DecodeArgs a{};
@@ -158,8 +161,10 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   a.page_size = page_size;
   a.num_blocks = (int)num_blocks;
   a.total_rows = (int)rows;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.out_scale = 1.f;
+  // an e4m3 row holds value / kv_scale: the scale folds into the scores and the output
+  const float kvs = cache_dtype == MLA_FP8_E4M3 ? kv_scale : 1.f;
+  a.scale_log2 = scale * 1.4426950408889634f * kvs;
+  a.out_scale = kvs;
   a.out = out;
   a.lse = lse;
   a.plan = mla::plan_from_workspace(workspace, L);

@@ -15,9 +15,9 @@
 //        those columns of the cached rows (plus the 64-dim box they straddle)
 //        and keeps its 288 query dims in TMEM as the A operand;
 //      - half of the output, dims [256r, 256r+256) of O += P . V.
-//    Each CTA computes a partial score tile S_r (18 MMAs, N = 64 keys), sends
-//    it to the peer as fp16 with one bulk shared-memory copy over the cluster
-//    network, and adds the peer's partial to its own (fp32) partial.  Nothing
+//    Each CTA computes a partial score tile S_r (18 MMAs, N = 64 keys), stores
+//    it into the peer's shared memory as fp16 (st.async over the cluster
+//    network), and adds the peer's partial to its own (fp32) partial.  Nothing
 //    is computed twice and every cached byte is read from HBM once.
 //  * The exchange of tile i+1 is issued before tile i is processed, so the
 //    network transfer overlaps the softmax of the previous tile.
@@ -38,6 +38,7 @@
 //    without touching memory outside its buffers.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -47,10 +48,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kStages = 4;                        // ring depth (query items and cache tiles)
 constexpr int kBox = 64 * 128;                    // 64 rows x 64 bf16 (128 B rows, 128-B swizzle)
 constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 column boxes
 constexpr int kStageBytes = kBoxesPerStage * kBox;
+constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
+constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
+constexpr int kFp8Slots = 3;                      // e4m3 staging ring (loads run 2 tiles ahead)
+// bf16 ring depth: 4 for a bf16 cache; 3 for e4m3 (the staging ring takes the rest)
+template <int kCacheFp8>
+struct Layout {
+  static constexpr int kStages = kCacheFp8 ? 3 : 4;
+  static constexpr int kStagingBytes = kCacheFp8 ? kFp8Slots * kFp8TileBytes : 0;
+};
 constexpr int kXBytes = kRows * kTile * 2;        // one fp16 partial score tile
 constexpr int kNumThreads = 224;
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
@@ -63,9 +72,12 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 static_assert(kTmemP + kTile / 2 <= 512, "TMEM columns");
 
+constexpr int kMaxStages = 4;
+
 struct __align__(8) Barriers {
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];   // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];  // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
+  uint64_t stg_full[kFp8Slots];   // e4m3 tile landed in the staging ring
   uint64_t q_ready;
   uint64_t s_full;
   uint64_t s_free;
@@ -80,7 +92,12 @@ struct __align__(8) Barriers {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 4 * (size_t)kXBytes + sizeof(Barriers);
+template <int kCacheFp8>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Layout<kCacheFp8>::kStages * kStageBytes + Layout<kCacheFp8>::kStagingBytes +
+         2 * (size_t)kXBytes + sizeof(Barriers);
+}
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
 
 struct Ctx {
   Barriers* bars;
@@ -140,15 +157,44 @@ __device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
   return rank == 0 ? (p < 4 || k < 2) : (p > 0 || k >= 2);
 }
 
+// Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major) into the bf16
+// 128-byte-swizzled layout the MMAs read (what a bf16 TMA load would have
+// written).  e4m3 -> f16 -> f32 -> bf16 is exact: every e4m3 value is a bf16
+// value.  Runs on the 32 lanes of the producer warp.
+__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int lane) {
+#pragma unroll 4
+  for (int i = lane; i < kBoxesPerStage * 64 * 4; i += 32) {
+    const int q = i & 3;               // 16-value chunk inside the 64-value row
+    const int r = (i >> 2) & 63;       // row (key)
+    const int p = i >> 8;              // box
+    const uint4 v = lds128(src + p * kFp8Box + r * 64 + q * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xFFFF), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
+      const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      o[2 * k] = pack_bf16x2(flo.x, flo.y);
+      o[2 * k + 1] = pack_bf16x2(fhi.x, fhi.y);
+    }
+    const uint32_t row = dst + p * kBox + r * 128;
+    sts128(row + (((2 * q) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+    sts128(row + (((2 * q + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
+  }
+}
+
 template <int kCacheFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
                   const __grid_constant__ CUtensorMap tm_kv, const DecodeArgs a) {
+  constexpr int kStages = Layout<kCacheFp8>::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
-  uint8_t* x_send = stages + kStages * kStageBytes;      // 2 buffers
-  uint8_t* x_recv = x_send + 2 * kXBytes;                 // 2 buffers
+  uint8_t* staging = stages + kStages * kStageBytes;     // e4m3 tiles (fp8 cache only)
+  uint8_t* x_recv = staging + Layout<kCacheFp8>::kStagingBytes;   // 2 receive buffers
   Barriers* bars = reinterpret_cast<Barriers*>(x_recv + 2 * kXBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,6 +209,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       mbar_init(smem_u32(&bars->kv_full[i]), 1);
       mbar_init(smem_u32(&bars->kv_empty[i]), 2);
     }
+    for (int i = 0; i < kFp8Slots; ++i) mbar_init(smem_u32(&bars->stg_full[i]), 1);
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), 4);
@@ -197,16 +244,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t item = 0;
+    // bf16 cache: lane 0 streams everything with TMA.  e4m3 cache: lane 0
+    // streams e4m3 tiles two ahead into the staging ring and the whole warp
+    // expands each one into the bf16 ring slot the MMAs read.
+    const bool leader = lane == 0;
+    if (kCacheFp8 || leader) {
+      uint32_t item = 0, g = 0;
       const int sub_rows = a.page_size < kTile ? a.page_size : kTile;
       const int nsub = kTile / sub_rows;
       const int oob_row = a.num_blocks * a.page_size;  // first row past the cache: reads zeros
       for (int u = ubeg; u < uend; ++u) {
         const UnitRec ur = P.units[u];
         const GroupRec gr = P.groups[ur.group];
+        const int32_t* bt = a.block_table + (size_t)gr.b * a.max_pages;
+        // loads the CTA's 5 column boxes of tile j (all sub-pages) into dst, counting on `full`
+        auto load_tile = [&](int j, uint32_t dst, uint32_t full, int row_bytes) {
+          for (int sb = 0; sb < nsub; ++sb) {
+            const int key = j * kTile + sb * sub_rows;
+            const int lp = key / a.page_size;
+            int y = oob_row;                 // sub-pages past the group's last key are not read
+            if (key < gr.lmax && lp < a.max_pages) {
+              const int blk = bt[lp];
+              if (blk >= 0 && blk < a.num_blocks)
+                y = blk * a.page_size + key % a.page_size;
+              else
+                atomicOr(ctx.status, 4);
+            }
+            const int box_bytes = 64 * row_bytes;
+            for (int p = 0; p < kBoxesPerStage; ++p)
+              tma_load_2d(dst + p * box_bytes + sb * sub_rows * row_bytes, &tm_kv, 256 * rank + 64 * p, y, full);
+          }
+        };
+        auto load_fp8 = [&](int j, uint32_t gg) {   // e4m3 tile j -> staging slot gg % kFp8Slots
+          const uint32_t full = smem_u32(&bars->stg_full[gg % kFp8Slots]);
+          mbar_expect_tx(full, kFp8TileBytes);
+          load_tile(j, smem_u32(staging + (gg % kFp8Slots) * kFp8TileBytes), full, 64);
+        };
+        const int ntiles = ur.tile_end - ur.tile_begin;
+        if (kCacheFp8 && leader)
+          for (int k = 0; k < ntiles && k < kFp8Slots - 1; ++k) load_fp8(ur.tile_begin + k, g + k);
         // the CTA's 288 query dims (5 boxes of 64) for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
+          if (!leader) continue;
           const uint32_t slot = item % kStages, round = item / kStages;
           wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
@@ -220,32 +299,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
               tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
           }
         }
-        const int32_t* bt = a.block_table + (size_t)gr.b * a.max_pages;
-        for (int j = ur.tile_begin; j < ur.tile_end; ++j, ++item) {
+        for (int jj = 0; jj < ntiles; ++jj, ++item) {
           const uint32_t slot = item % kStages, round = item / kStages;
-          wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
-          const uint32_t st = smem_u32(stages + slot * kStageBytes);
-          const uint32_t full = smem_u32(&bars->kv_full[slot]);
-          mbar_expect_tx(full, kStageBytes);
-          for (int sb = 0; sb < nsub; ++sb) {
-            const int key = j * kTile + sb * sub_rows;
-            const int lp = key / a.page_size;
-            int y = oob_row;                 // sub-pages past the group's last key are not read
-            if (key < gr.lmax && lp < a.max_pages) {
-              const int blk = bt[lp];
-              if (blk >= 0 && blk < a.num_blocks)
-                y = blk * a.page_size + key % a.page_size;
-              else
-                atomicOr(ctx.status, 4);
-            }
-            const uint32_t dst = st + sb * sub_rows * 128;
-            for (int p = 0; p < kBoxesPerStage; ++p) tma_load_2d(dst + p * kBox, &tm_kv, 256 * rank + 64 * p, y, full);
+          if (!kCacheFp8) {
+            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+            const uint32_t full = smem_u32(&bars->kv_full[slot]);
+            mbar_expect_tx(full, kStageBytes);
+            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full, 128);
+          } else {
+            if (leader && jj + kFp8Slots - 1 < ntiles) load_fp8(ur.tile_begin + jj + kFp8Slots - 1, g + kFp8Slots - 1);
+            wait_bar(ctx, &bars->stg_full[g % kFp8Slots], (g / kFp8Slots) & 1);
+            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+            __syncwarp();
+            expand_e4m3_tile(smem_u32(staging + (g % kFp8Slots) * kFp8TileBytes), smem_u32(stages + slot * kStageBytes),
+                             lane);
+            fence_proxy_async_smem();    // bf16 writes visible to the MMAs; staging reads ordered before reuse
+            __syncwarp();
+            if (leader) mbar_arrive(smem_u32(&bars->kv_full[slot]));
+            ++g;
           }
         }
       }
       // drain: every issued load has landed before the CTA may exit
-      const uint32_t first = item > kStages ? item - kStages : 0;
-      for (uint32_t k = first; k < item; ++k) mbar_wait(smem_u32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
+      if (leader) {
+        const uint32_t first = item > kStages ? item - kStages : 0;
+        for (uint32_t k = first; k < item; ++k) mbar_wait(smem_u32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -323,11 +402,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
     const int tid128 = threadIdx.x - 96;
     const uint32_t xrow = (uint32_t)row * (kTile * 2);
-    const uint32_t xsend0 = smem_u32(x_send), xrecv0 = smem_u32(x_recv);
+    const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
     const uint32_t xfree_peer0 = mapa(smem_u32(&bars->x_free[0]), peer);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
     // Load partial scores of tile `t` from TMEM into `dst` and free the S columns.
     auto load_s = [&](uint32_t t, float (&dst)[kTile]) {
@@ -347,23 +427,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
     };
-    // Send partial scores of tile `t` (fp16, valid rows only) to the peer.
-    auto send_s = [&](uint32_t t, const float (&src)[kTile], uint32_t nbytes) {
+    // Send partial scores of tile `t` (fp16, valid rows only) straight into the
+    // peer's receive buffer: 16-byte st.async stores that count against the
+    // peer's barrier (this keeps the exchange off the TMA engine that streams
+    // the cache tiles).
+    auto send_s = [&](uint32_t t, const float (&src)[kTile]) {
       const uint32_t b = t & 1, use = t >> 1;
-      if (tid128 == 0) bulk_wait_group_read<1>();    // the copy of tile t-2 no longer reads buffer b
-      named_bar_softmax();
-      const uint32_t base = xsend0 + b * kXBytes + xrow;
+      wait_bar_cluster(ctx, &bars->x_free[b], (use & 1) ^ 1);   // the peer consumed tile t-2 from buffer b
+      __syncwarp();
+      if (row < nrows_cur) {
+        const uint32_t base = xrecv_peer0 + b * kXBytes + xrow;
+        const uint32_t bar = xfull_peer0 + b * 8;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        sts128(base + ((c ^ (row & 7)) << 4), pack_f16x2(src[8 * c], src[8 * c + 1]),
-               pack_f16x2(src[8 * c + 2], src[8 * c + 3]), pack_f16x2(src[8 * c + 4], src[8 * c + 5]),
-               pack_f16x2(src[8 * c + 6], src[8 * c + 7]));
-      fence_proxy_async_smem();
-      named_bar_softmax();
-      if (tid128 == 0) {
-        wait_bar_cluster(ctx, &bars->x_free[b], (use & 1) ^ 1);
-        bulk_copy_to_peer(xrecv_peer0 + b * kXBytes, xsend0 + b * kXBytes, nbytes, xfull_peer0 + b * 8);
-        bulk_commit_group();
+        for (int c = 0; c < 8; ++c)
+          st_async_v4(base + ((c ^ (row & 7)) << 4), pack_f16x2(src[8 * c], src[8 * c + 1]),
+                      pack_f16x2(src[8 * c + 2], src[8 * c + 3]), pack_f16x2(src[8 * c + 4], src[8 * c + 5]),
+                      pack_f16x2(src[8 * c + 6], src[8 * c + 7]), bar);
       }
     };
     // Add the peer's partial scores of tile `t` into `acc`.
@@ -387,7 +466,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         acc[8 * c + 7] += f3.y;
       }
       named_bar_softmax();
-      if (tid128 == 0) mbar_arrive_remote(xfree_peer0 + b * 8);
+      if (tid128 == 0) mbar_arrive_remote(xfree_peer0 + b * 8);   // all rows read: buffer b is free again
     };
 
     uint32_t item = 0, it = 0, units_done = 0;
@@ -395,6 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       const UnitRec ur = P.units[u];
       const GroupRec gr = P.groups[ur.group];
       const int b = gr.b;
+      nrows_cur = gr.nrows;
       const int sq = a.qsl ? a.qsl[b + 1] - a.qsl[b] : 1;
       const int q0 = a.qsl ? a.qsl[b] : b;
       const int R = gr.row0 + row;
@@ -459,13 +539,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       float cur[kTile], nxt[kTile];
       if (ntiles > 0) {
         load_s(it, cur);
-        send_s(it, cur, nbytes);
+        send_s(it, cur);
       }
       for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
         // exchange of the next tile first: the network copy overlaps this tile's work
         if (jj + 1 < ntiles) {
           load_s(it + 1, nxt);
-          send_s(it + 1, nxt, nbytes);
+          send_s(it + 1, nxt);
         }
         recv_s(it, cur, nbytes);
 
@@ -565,7 +645,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       }
       tc_fence_before();
     }
-    if (tid128 == 0) bulk_wait_group_read<0>();
   }
 
   __syncthreads();
@@ -578,15 +657,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 
 }  // namespace
 
-size_t decode_smem_bytes(int) { return kSmemBytes; }
+size_t decode_smem_bytes(int cache_dtype) { return cache_dtype ? smem_bytes<1>() : smem_bytes<0>(); }
 
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
                           int cache_dtype, const DecodeArgs& a, int num_clusters, cudaStream_t s) {
-  (void)cache_dtype;
-  auto kern = decode_kernel<0>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  const size_t smem = decode_smem_bytes(cache_dtype);
+  auto kern = cache_dtype ? decode_kernel<1> : decode_kernel<0>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<2 * num_clusters, kNumThreads, kSmemBytes, s>>>(tm_q, tm_qpe, tm_kv, a);
+  kern<<<2 * num_clusters, kNumThreads, smem, s>>>(tm_q, tm_qpe, tm_kv, a);
   return cudaGetLastError();
 }
 

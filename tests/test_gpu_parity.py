@@ -109,6 +109,20 @@ def test_decode_small_cases(num_heads, sq, page_size, num_splits):
     assert mla.decode_status(g.workspace) == 0
 
 
+@pytest.mark.parametrize("num_heads,sq,page_size,num_splits", [
+    (128, 1, 64, 0), (16, 1, 64, 3), (128, 4, 64, 0), (128, [4, 1, 1, 2, 1, 3], 16, 2),
+])
+def test_decode_fp8_cache(num_heads, sq, page_size, num_splits):
+    """e4m3 cache with a per-tensor scale, dequantised inside the decode; against
+    the oracle run on the dequantised values."""
+    case = synth.make_decode_case(num_heads=num_heads, batch=6, ctx=(60, 700), sq=sq, page_size=page_size,
+                                  cache_dtype="fp8", seed=200 + num_heads + page_size + num_splits)
+    g = GpuCase(case, num_splits_max=num_splits)
+    g.decode(num_splits)
+    compare(case, g)
+    assert mla.decode_status(g.workspace) == 0
+
+
 def test_decode_edge_lengths():
     """seq_len 0 (padding request), Sq > seq_len, one-token contexts, exact
     multiples of the tile, lengths one past a tile."""
@@ -163,7 +177,7 @@ def test_block_id_out_of_range_flags_and_does_not_fault():
 
 # --------------------------------------------------------- full-size workloads
 
-FULL = [("dsv3_n128_b64_ctx1k-8k", (0,)), ("n16_b128_ctx8k-32k", (0, 4, 16)),
+FULL = [("dsv3_n128_b64_ctx1k-8k", (0,)), ("dsv3_n128_b64_ctx1k-8k_fp8", (0,)), ("n16_b128_ctx8k-32k", (0, 4, 16)),
         ("mtp_n128_sq4_b32_ctx2k-16k", (0,)), ("mtp_mixed_n128_b32_ctx2k-16k", (0,))]
 
 
