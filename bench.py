@@ -43,6 +43,30 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def decode_source_hash() -> str:
+    import hashlib
+    src = os.path.join(ROOT, "mla_latent_kv_15_gb300", "csrc", "decode.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload, if that summary was taken on the current decode kernel source."""
+    for name in (f"decode_{workload}.md", f"decode_{workload}_bf16.md"):
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            continue
+        sha, traffic = None, None
+        for line in open(path):
+            if "Kernel source sha256" in line:
+                sha = line.strip().split()[-1]
+            if line.startswith("traffic_bytes_per_launch:"):
+                traffic = int(line.split(":")[1])
+        if sha == decode_source_hash():
+            return traffic
+    return None
+
+
 def algorithmic(case):
     """Bytes and FLOPs the decode must move / do at minimum: every visible
     latent row read once per request, queries read, outputs and LSE written;
@@ -238,6 +262,19 @@ def run_gpu(args):
     alg = algorithmic(case)
     hbm, tflops, src = peaks()
     achieved = alg["decode_bytes"] / (kms * 1e-3) / 1e9
+    achieved_tf = alg["flops"] / (kms * 1e-3) / 1e12
+    # the binding roof of the workload: bytes at the HBM peak or FLOPs at the bf16 tensor peak
+    hbm_bound = alg["decode_bytes"] / (hbm * 1e9) >= alg["flops"] / (tflops * 1e12)
+    traffic = profiled_traffic(args.workload)
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / tflops, 4)}
+    roof.update({"traffic": traffic,
+                 "peak_source": f"{src} (MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'})",
+                 "algorithmic_bytes_per_launch": alg["decode_bytes"], "algorithmic_flops_per_launch": alg["flops"]})
     tok_s = world * T / (ms * 1e-3)
     clocks = sampler.summary()
     res = {
@@ -260,14 +297,9 @@ def run_gpu(args):
             "l2": "flushed (256 MiB write) before every timed step",
         },
         "hbm_gbs": round(achieved, 1),
-        "tflops": round(alg["flops"] / (kms * 1e-3) / 1e12, 1),
+        "tflops": round(achieved_tf, 1),
         "decode_kernel_ms": round(kms, 5),
-        "roofline": {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-            "frac": round(achieved / hbm, 4), "traffic": None,
-            "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
-            "algorithmic_bytes_per_launch": alg["decode_bytes"],
-        },
+        "roofline": roof,
         "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": inp_bytes, "d2h_bytes_per_step": out_bytes},
         "gpu_launches": 4 * args.steps,

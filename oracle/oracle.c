@@ -22,7 +22,8 @@
  *    (num_blocks, block_size, head_size) (get_kv_cache_shape).  With Sq query
  *    tokens per request, query token t sees keys [0, seq_len - Sq + 1 + t)
  *    (vllm.v1.attention.backends.mla.rocm_aiter_mla, AiterMLAImpl.forward_mqa,
- *    multi-token verify: "Token t may attend to [0, context_r + t]").
+ *    multi-token verify: verify token t sees the context plus the new tokens
+ *    up to and including itself).
  *  - oracle_merge: merge_attn_states of two partial results over disjoint key
  *    sets (common.py docstring, "Chunked Prefill"); the formula is not
  *    printed on the pages, it is the softmax over the union of the key sets.

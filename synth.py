@@ -12,9 +12,9 @@ head_size) from ``get_kv_cache_shape``):
 
 * latent rows ``[kv_c | k_pe]`` (576 wide) and absorbed queries
   ``[q_abs | q_pe]`` are N(0,1)*0.5 drawn in float32, rounded to bf16 (RNE);
-* context lengths are uniform integers in [lo, hi] and count the new query
-  tokens of the step (seq_lens semantics of the AITER MLA backend,
-  ``forward_mqa``: "seq_lens counts the tokens scheduled in this step");
+* context lengths are uniform integers in [lo, hi] and include the new query
+  tokens of the step (the sequence-length convention of the AITER MLA
+  backend, ``forward_mqa``, multi-token verify path);
 * block tables are disjoint slices of one random permutation of the page pool;
   unused table entries are -1;
 * the new latent rows of the step (one per query token) go to the slots of the
