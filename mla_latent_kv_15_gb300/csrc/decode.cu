@@ -20,7 +20,11 @@
 //    network), and adds the peer's partial to its own (fp32) partial.  Nothing
 //    is computed twice and every cached byte is read from HBM once.
 //  * The exchange of tile i+1 is issued before tile i is processed, so the
-//    network transfer overlaps the softmax of the previous tile.
+//    network transfer overlaps the softmax of the previous tile.  Partials
+//    land in a ring of four receive buffers that needs no return handshake:
+//    a CTA writes tile i+1 into the buffer of tile i-3 only after it has
+//    received tile i-1 from the peer, and the peer sent tile i-1 only after
+//    all its softmax threads had read tile i-3.
 //  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
 //    bf16 P (A operand of P.V) [464,496).
 //  * Warp roles: warp 0 TMA producer; warp 1 score-MMA issuer (+TMEM owner);
@@ -53,7 +57,7 @@ constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 c
 constexpr int kStageBytes = kBoxesPerStage * kBox;
 constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
 constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
-constexpr int kFp8Slots = 3;                      // e4m3 staging ring (loads run 2 tiles ahead)
+constexpr int kFp8Slots = 2;                      // e4m3 staging ring (loads run 1 tile ahead)
 // bf16 ring depth: 4 for a bf16 cache; 3 for e4m3 (the staging ring takes the rest)
 template <int kCacheFp8>
 struct Layout {
@@ -61,6 +65,7 @@ struct Layout {
   static constexpr int kStagingBytes = kCacheFp8 ? kFp8Slots * kFp8TileBytes : 0;
 };
 constexpr int kXBytes = kRows * kTile * 2;        // one fp16 partial score tile
+constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
 constexpr int kNumThreads = 224;
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
 
@@ -84,8 +89,7 @@ struct __align__(8) Barriers {
   uint64_t p_full;
   uint64_t p_free;
   uint64_t o_full;
-  uint64_t x_full[2];           // peer's partial scores landed (transaction count)
-  uint64_t x_free[2];           // the peer has consumed what we sent into its buffer
+  uint64_t x_full[kXBuffers];   // peer's partial scores landed (transaction count)
   uint64_t s_drain;
   uint64_t p_drain;
   uint32_t tmem_base;
@@ -95,7 +99,7 @@ struct __align__(8) Barriers {
 template <int kCacheFp8>
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)Layout<kCacheFp8>::kStages * kStageBytes + Layout<kCacheFp8>::kStagingBytes +
-         2 * (size_t)kXBytes + sizeof(Barriers);
+         kXBuffers * (size_t)kXBytes + sizeof(Barriers);
 }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
 
@@ -194,8 +198,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
   uint8_t* staging = stages + kStages * kStageBytes;     // e4m3 tiles (fp8 cache only)
-  uint8_t* x_recv = staging + Layout<kCacheFp8>::kStagingBytes;   // 2 receive buffers
-  Barriers* bars = reinterpret_cast<Barriers*>(x_recv + 2 * kXBytes);
+  uint8_t* x_recv = staging + Layout<kCacheFp8>::kStagingBytes;   // receive ring
+  Barriers* bars = reinterpret_cast<Barriers*>(x_recv + kXBuffers * kXBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -216,10 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     mbar_init(smem_u32(&bars->p_full), 4);
     mbar_init(smem_u32(&bars->p_free), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->x_full[i]), 1);
-      mbar_init(smem_u32(&bars->x_free[i]), 1);
-    }
+    for (int i = 0; i < kXBuffers; ++i) mbar_init(smem_u32(&bars->x_full[i]), 1);
     mbar_init(smem_u32(&bars->s_drain), 1);
     mbar_init(smem_u32(&bars->p_drain), 1);
     bars->abort = 0;
@@ -405,7 +406,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
-    const uint32_t xfree_peer0 = mapa(smem_u32(&bars->x_free[0]), peer);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
@@ -432,9 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     // peer's barrier (this keeps the exchange off the TMA engine that streams
     // the cache tiles).
     auto send_s = [&](uint32_t t, const float (&src)[kTile]) {
-      const uint32_t b = t & 1, use = t >> 1;
-      wait_bar_cluster(ctx, &bars->x_free[b], (use & 1) ^ 1);   // the peer consumed tile t-2 from buffer b
-      __syncwarp();
+      const uint32_t b = t % kXBuffers;
       if (row < nrows_cur) {
         const uint32_t base = xrecv_peer0 + b * kXBytes + xrow;
         const uint32_t bar = xfull_peer0 + b * 8;
@@ -447,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     };
     // Add the peer's partial scores of tile `t` into `acc`.
     auto recv_s = [&](uint32_t t, float (&acc)[kTile], uint32_t nbytes) {
-      const uint32_t b = t & 1, use = t >> 1;
+      const uint32_t b = t % kXBuffers, use = t / kXBuffers;
       if (tid128 == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
       wait_bar_cluster(ctx, &bars->x_full[b], use & 1);
       __syncwarp();
@@ -465,8 +463,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         acc[8 * c + 6] += f3.x;
         acc[8 * c + 7] += f3.y;
       }
+      // every row of buffer b is read before any thread sends its row of a
+      // later tile: a received tile then proves the peer is done with the
+      // buffer three tiles back, whatever the row counts of the units
       named_bar_softmax();
-      if (tid128 == 0) mbar_arrive_remote(xfree_peer0 + b * 8);   // all rows read: buffer b is free again
     };
 
     uint32_t item = 0, it = 0, units_done = 0;
