@@ -240,6 +240,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
 
+  // everything above overlaps the plan kernel (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int ubeg = P.cluster_begin[cluster];
   const int uend = P.cluster_begin[cluster + 1];
 
@@ -665,7 +667,20 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, co
   auto kern = cache_dtype ? decode_kernel<1> : decode_kernel<0>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<2 * num_clusters, kNumThreads, smem, s>>>(tm_q, tm_qpe, tm_kv, a);
+  // programmatic dependent launch: the prologue (barriers, TMEM, cluster
+  // sync) overlaps the plan kernel; the kernel waits for it before reading the plan
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_clusters);
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qpe, tm_kv, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -18,6 +18,8 @@ namespace {
 // Grid (groups, 32): block (g, y) merges rows 4y..4y+3 of group g, 64
 // threads per row, 8 dims per thread.
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
+  // launched as a programmatic dependent of the decode kernel: wait for it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const Plan& P = a.plan;
   const int g = blockIdx.x;
   if (g >= P.header->num_groups) return;
@@ -146,7 +148,17 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s) {
-  combine_kernel<<<dim3(max_groups, kRows / 4), 256, 0, s>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(max_groups, kRows / 4);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
