@@ -27,10 +27,11 @@
 //    all its softmax threads had read tile i-3.
 //  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
 //    bf16 P (A operand of P.V) [464,496).
-//  * Warp roles: warp 0 TMA producer; warp 1 score-MMA issuer (+TMEM owner);
-//    warp 2 P.V-MMA issuer; warps 3-6 softmax / exchange / O rescale /
-//    epilogue (one query row per thread, the row's TMEM lane).  Two issuer
-//    warps, because one thread issues at most one MMA per ~48 cycles.
+//  * Warp roles: a TMA producer, a score-MMA issuer (+TMEM owner), a P.V-MMA
+//    issuer, four softmax / exchange / O rescale / epilogue warps (one query
+//    row per thread, the row's TMEM lane) and, for an e4m3 cache, four warps
+//    that expand e4m3 tiles to bf16 (see Roles).  Separate score and P.V
+//    issuers let the two MMA accumulation chains overlap in the tensor pipe.
 //  * Online softmax in the exp2 domain with lazy rescaling: O and l are
 //    rescaled only when a row's running max grows by more than 8 (log2
 //    units); the final o = O / l and lse = (m + log2 l) ln 2 are exact for
@@ -57,7 +58,7 @@ constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 c
 constexpr int kStageBytes = kBoxesPerStage * kBox;
 constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
 constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
-constexpr int kFp8Slots = 2;                      // e4m3 staging ring (loads run 1 tile ahead)
+constexpr int kFp8Slots = 2;                      // e4m3 staging ring (two tiles in flight)
 // bf16 ring depth: 4 for a bf16 cache; 3 for e4m3 (the staging ring takes the rest)
 template <int kCacheFp8>
 struct Layout {
@@ -66,7 +67,25 @@ struct Layout {
 };
 constexpr int kXBytes = kRows * kTile * 2;        // one fp16 partial score tile
 constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
-constexpr int kNumThreads = 224;
+// Warp roles.
+//  bf16 cache (224 threads): 0 TMA producer, 1 score-MMA issuer (and TMEM
+//    owner), 2 P.V-MMA issuer, 3-6 softmax.
+//  e4m3 cache (384 threads, grouped by warpgroup so that each group gets its
+//    own register budget): 0-3 softmax, 4-7 e4m3 expansion, 8 TMA producer,
+//    9 score-MMA issuer, 10 P.V-MMA issuer, 11 idle.
+template <int kCacheFp8>
+struct Roles {
+  static constexpr int kThreads = kCacheFp8 ? 384 : 224;
+  static constexpr int kSoftmax0 = kCacheFp8 ? 0 : 3;
+  static constexpr int kProducer = kCacheFp8 ? 8 : 0;
+  static constexpr int kScore = kCacheFp8 ? 9 : 1;
+  static constexpr int kPV = kCacheFp8 ? 10 : 2;
+};
+constexpr int kWarpExpand0 = 4;   // e4m3 cache only
+// e4m3 registers per thread after the split (launch: 168): 128 x (248 + 88 +
+// 112) = 57344 stay within the 384 x 168 the CTA is launched with.
+constexpr uint32_t kRegsSoftmax = 248, kRegsExpand = 88, kRegsIssue = 112;
+static_assert(128 * (kRegsSoftmax + kRegsExpand + kRegsIssue) <= 384 * 168, "register split");
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
 
 constexpr uint32_t kTmemO = 0;
@@ -83,6 +102,7 @@ struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];  // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
   uint64_t stg_full[kFp8Slots];   // e4m3 tile landed in the staging ring
+  uint64_t stg_empty[kFp8Slots];  // the expansion warps are done with a staging slot
   uint64_t q_ready;
   uint64_t s_full;
   uint64_t s_free;
@@ -124,6 +144,7 @@ __device__ __forceinline__ void wait_bar_cluster(const Ctx& c, uint64_t* bar, ui
 }
 
 __device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_expand() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -164,10 +185,10 @@ __device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
 // Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major) into the bf16
 // 128-byte-swizzled layout the MMAs read (what a bf16 TMA load would have
 // written).  e4m3 -> f16 -> f32 -> bf16 is exact: every e4m3 value is a bf16
-// value.  Runs on the 32 lanes of the producer warp.
-__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int lane) {
-#pragma unroll 4
-  for (int i = lane; i < kBoxesPerStage * 64 * 4; i += 32) {
+// value.  Runs on the 128 threads of the expansion warps.
+__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int t) {
+#pragma unroll 2
+  for (int i = t; i < kBoxesPerStage * 64 * 4; i += 128) {
     const int q = i & 3;               // 16-value chunk inside the 64-value row
     const int r = (i >> 2) & 63;       // row (key)
     const int p = i >> 8;              // box
@@ -190,7 +211,7 @@ __device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int
 }
 
 template <int kCacheFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kCacheFp8>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
                   const __grid_constant__ CUtensorMap tm_kv, const DecodeArgs a) {
   constexpr int kStages = Layout<kCacheFp8>::kStages;
@@ -213,7 +234,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       mbar_init(smem_u32(&bars->kv_full[i]), 1);
       mbar_init(smem_u32(&bars->kv_empty[i]), 2);
     }
-    for (int i = 0; i < kFp8Slots; ++i) mbar_init(smem_u32(&bars->stg_full[i]), 1);
+    for (int i = 0; i < kFp8Slots; ++i) {
+      mbar_init(smem_u32(&bars->stg_full[i]), 1);
+      mbar_init(smem_u32(&bars->stg_empty[i]), 1);
+    }
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), 4);
@@ -226,11 +250,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  using R = Roles<kCacheFp8>;
+  if (warp == R::kScore) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == R::kProducer && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_qpe);
     tma_prefetch_desc(&tm_kv);
@@ -245,13 +270,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   const int ubeg = P.cluster_begin[cluster];
   const int uend = P.cluster_begin[cluster + 1];
 
-  if (warp == 0) {
+  // Role bodies; the dispatch below differs per cache type: with an e4m3
+  // cache each warpgroup first sets its register budget, so the compiler
+  // allocates every role's code against that budget.
+  auto producer = [&]() {
     // ------------------------------------------------------------ producer
-    // bf16 cache: lane 0 streams everything with TMA.  e4m3 cache: lane 0
-    // streams e4m3 tiles two ahead into the staging ring and the whole warp
-    // expands each one into the bf16 ring slot the MMAs read.
+    // Lane 0 streams everything with TMA: bf16 tiles straight into the ring;
+    // e4m3 tiles into the staging ring, which the expansion warps turn into
+    // the bf16 ring slots the MMAs read.
     const bool leader = lane == 0;
-    if (kCacheFp8 || leader) {
+    if (leader) {
       uint32_t item = 0, g = 0;
       const int sub_rows = a.page_size < kTile ? a.page_size : kTile;
       const int nsub = kTile / sub_rows;
@@ -278,14 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
               tma_load_2d(dst + p * box_bytes + sb * sub_rows * row_bytes, &tm_kv, 256 * rank + 64 * p, y, full);
           }
         };
-        auto load_fp8 = [&](int j, uint32_t gg) {   // e4m3 tile j -> staging slot gg % kFp8Slots
-          const uint32_t full = smem_u32(&bars->stg_full[gg % kFp8Slots]);
-          mbar_expect_tx(full, kFp8TileBytes);
-          load_tile(j, smem_u32(staging + (gg % kFp8Slots) * kFp8TileBytes), full, 64);
-        };
         const int ntiles = ur.tile_end - ur.tile_begin;
-        if (kCacheFp8 && leader)
-          for (int k = 0; k < ntiles && k < kFp8Slots - 1; ++k) load_fp8(ur.tile_begin + k, g + k);
         // the CTA's 288 query dims (5 boxes of 64) for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
           if (!leader) continue;
@@ -310,15 +331,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             mbar_expect_tx(full, kStageBytes);
             load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full, 128);
           } else {
-            if (leader && jj + kFp8Slots - 1 < ntiles) load_fp8(ur.tile_begin + jj + kFp8Slots - 1, g + kFp8Slots - 1);
-            wait_bar(ctx, &bars->stg_full[g % kFp8Slots], (g / kFp8Slots) & 1);
-            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
-            __syncwarp();
-            expand_e4m3_tile(smem_u32(staging + (g % kFp8Slots) * kFp8TileBytes), smem_u32(stages + slot * kStageBytes),
-                             lane);
-            fence_proxy_async_smem();    // bf16 writes visible to the MMAs; staging reads ordered before reuse
-            __syncwarp();
-            if (leader) mbar_arrive(smem_u32(&bars->kv_full[slot]));
+            const uint32_t sl = g % kFp8Slots;
+            wait_bar(ctx, &bars->stg_empty[sl], ((g / kFp8Slots) & 1) ^ 1);
+            const uint32_t full = smem_u32(&bars->stg_full[sl]);
+            mbar_expect_tx(full, kFp8TileBytes);
+            load_tile(ur.tile_begin + jj, smem_u32(staging + sl * kFp8TileBytes), full, 64);
             ++g;
           }
         }
@@ -330,7 +347,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
+  };
+  auto score_issuer = [&]() {
     // ---------------------------------------------------- score-MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, 0, 0);   // K-major keys, N = 64
@@ -367,7 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       mbar_wait(smem_u32(&bars->s_drain), 0);
     }
     __syncwarp();
-  } else if (warp == 2) {
+  };
+  auto pv_issuer = [&]() {
     // ------------------------------------------------------ P.V-MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, 0, 1);    // MN-major values, N = 256
@@ -398,12 +417,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       mbar_wait(smem_u32(&bars->p_drain), 0);
     }
     __syncwarp();
-  } else {
+  };
+  auto expander = [&]() {
+    // -------------------------------------------------------- e4m3 expansion
+    const int te = threadIdx.x - 32 * kWarpExpand0;
+    uint32_t item = 0, g = 0;
+    for (int u = ubeg; u < uend; ++u) {
+      const UnitRec ur = P.units[u];
+      const int ntiles = ur.tile_end - ur.tile_begin;
+      item += 2;  // the query items are loaded by the producer
+      for (int jj = 0; jj < ntiles; ++jj, ++item, ++g) {
+        const uint32_t slot = item % kStages, round = item / kStages;
+        const uint32_t sl = g % kFp8Slots;
+        wait_bar(ctx, &bars->stg_full[sl], (g / kFp8Slots) & 1);
+        wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+        expand_e4m3_tile(smem_u32(staging + sl * kFp8TileBytes), smem_u32(stages + slot * kStageBytes), te);
+        fence_proxy_async_smem();    // bf16 writes visible to the MMAs; staging reads done before reuse
+        named_bar_expand();
+        if (te == 0) {
+          mbar_arrive(smem_u32(&bars->kv_full[slot]));
+          mbar_arrive(smem_u32(&bars->stg_empty[sl]));
+        }
+      }
+    }
+  };
+  auto softmax = [&]() {
     // ------------------------------------- softmax / exchange / rescale / epilogue
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
     const int row = q4 * 32 + lane;          // query row of this thread in the unit
     const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
-    const int tid128 = threadIdx.x - 96;
+    const int tid128 = threadIdx.x - 32 * R::kSoftmax0;
     const uint32_t xrow = (uint32_t)row * (kTile * 2);
     const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
@@ -647,10 +690,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       }
       tc_fence_before();
     }
+  };
+  if constexpr (kCacheFp8 != 0) {
+    if (warp >= R::kProducer) {
+      setmaxnreg_dec<kRegsIssue>();
+      if (warp == R::kProducer)
+        producer();
+      else if (warp == R::kScore)
+        score_issuer();
+      else if (warp == R::kPV)
+        pv_issuer();
+    } else if (warp >= kWarpExpand0) {
+      setmaxnreg_dec<kRegsExpand>();
+      expander();
+    } else {
+      setmaxnreg_inc<kRegsSoftmax>();
+      softmax();
+    }
+  } else {
+    if (warp == R::kProducer)
+      producer();
+    else if (warp == R::kScore)
+      score_issuer();
+    else if (warp == R::kPV)
+      pv_issuer();
+    else
+      softmax();
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == R::kScore) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -671,7 +740,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, co
   // sync) overlaps the plan kernel; the kernel waits for it before reading the plan
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
-  cfg.blockDim = dim3(kNumThreads);
+  cfg.blockDim = dim3(cache_dtype ? Roles<1>::kThreads : Roles<0>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
