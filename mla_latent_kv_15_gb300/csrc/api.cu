@@ -170,12 +170,17 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   a.plan = mla::plan_from_workspace(workspace, L);
 
   cudaStream_t s = (cudaStream_t)stream;
+  // small head counts with one query token per request (total_q == batch):
+  // 32-row groups and the decode variant with small receive buffers and a
+  // deeper cache ring.  Groups never outnumber the batch then: a request with
+  // Sq tokens gives ceil(Sq * N / 32) <= Sq groups.
+  const int small_rows = cache_dtype == MLA_BF16 && num_heads <= 32 && total_q == batch;
   cudaError_t e = mla::launch_plan(seq_lens, query_start_loc, batch, num_heads, max_pages_per_seq, page_size,
-                                   num_splits, clusters, a.plan, s);
+                                   num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
-  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, cache_dtype, a, clusters, s);
+  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, cache_dtype, small_rows, a, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
   e = mla::launch_combine(a, L.max_groups, s);

@@ -120,16 +120,18 @@ struct DecodeArgs {
 };
 
 // ---- launchers (return cudaError_t of the launch)
+// group_rows: query rows per group (128; 32 for the small-rows decode variant)
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
-                        int page_size, int num_splits, int num_clusters, Plan plan, cudaStream_t s);
+                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s);
+// small_rows: bf16 cache and every group has at most 32 rows (plan built with group_rows = 32)
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
-                          int cache_dtype, const DecodeArgs& a, int num_clusters, cudaStream_t s);
+                          int cache_dtype, int small_rows, const DecodeArgs& a, int num_clusters, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                                 int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,
                                 cudaStream_t s);
 cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
                                void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s);
-size_t decode_smem_bytes(int cache_dtype);
+size_t decode_smem_bytes(int variant);
 
 }  // namespace mla

@@ -59,14 +59,18 @@ constexpr int kStageBytes = kBoxesPerStage * kBox;
 constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
 constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
 constexpr int kFp8Slots = 2;                      // e4m3 staging ring (two tiles in flight)
-// bf16 ring depth: 4 for a bf16 cache; 3 for e4m3 (the staging ring takes the rest)
-template <int kCacheFp8>
+// Kernel variants: 0 bf16 cache; 1 e4m3 cache; 2 bf16 cache with at most 32
+// query rows per unit (small head counts: the receive ring shrinks to 32-row
+// buffers and the cache ring gets a fifth stage).
+template <int kVariant>
 struct Layout {
-  static constexpr int kStages = kCacheFp8 ? 3 : 4;
-  static constexpr int kStagingBytes = kCacheFp8 ? kFp8Slots * kFp8TileBytes : 0;
+  static constexpr int kStages = kVariant == 1 ? 3 : (kVariant == 2 ? 5 : 4);
+  static constexpr int kStagingBytes = kVariant == 1 ? kFp8Slots * kFp8TileBytes : 0;
+  static constexpr int kXRows = kVariant == 2 ? 32 : kRows;        // rows of a receive buffer
+  static constexpr int kXBytes = kXRows * kTile * 2;              // one fp16 partial score tile
 };
-constexpr int kXBytes = kRows * kTile * 2;        // one fp16 partial score tile
 constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
+constexpr int kSmallRows = 32;                    // unit rows of variant 2
 // Warp roles.
 //  bf16 cache (224 threads): 0 TMA producer, 1 score-MMA issuer (and TMEM
 //    owner), 2 P.V-MMA issuer, 3-6 softmax.
@@ -96,7 +100,7 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units
 
 static_assert(kTmemP + kTile / 2 <= 512, "TMEM columns");
 
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 5;
 
 struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
@@ -116,12 +120,15 @@ struct __align__(8) Barriers {
   int abort;
 };
 
-template <int kCacheFp8>
+template <int kVariant>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Layout<kCacheFp8>::kStages * kStageBytes + Layout<kCacheFp8>::kStagingBytes +
-         kXBuffers * (size_t)kXBytes + sizeof(Barriers);
+  return 1024 + (size_t)Layout<kVariant>::kStages * kStageBytes + Layout<kVariant>::kStagingBytes +
+         kXBuffers * (size_t)Layout<kVariant>::kXBytes + sizeof(Barriers);
 }
-static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448, "shared memory per CTA");
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
+              "shared memory per CTA");
+static_assert(Layout<0>::kStages <= kMaxStages && Layout<1>::kStages <= kMaxStages && Layout<2>::kStages <= kMaxStages,
+              "barrier arrays");
 
 struct Ctx {
   Barriers* bars;
@@ -210,16 +217,19 @@ __device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int
   }
 }
 
-template <int kCacheFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kCacheFp8>::kThreads, 1)
+template <int kVariant>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
                   const __grid_constant__ CUtensorMap tm_kv, const DecodeArgs a) {
-  constexpr int kStages = Layout<kCacheFp8>::kStages;
+  constexpr int kCacheFp8 = kVariant == 1;
+  constexpr int kStages = Layout<kVariant>::kStages;
+  constexpr int kXBytes = Layout<kVariant>::kXBytes;
+  constexpr int kXRows = Layout<kVariant>::kXRows;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
   uint8_t* staging = stages + kStages * kStageBytes;     // e4m3 tiles (fp8 cache only)
-  uint8_t* x_recv = staging + Layout<kCacheFp8>::kStagingBytes;   // receive ring
+  uint8_t* x_recv = staging + Layout<kVariant>::kStagingBytes;   // receive ring
   Barriers* bars = reinterpret_cast<Barriers*>(x_recv + kXBuffers * kXBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -496,7 +506,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kCacheFp8>::kT
       __syncwarp();
       const uint32_t base = xrecv0 + b * kXBytes + xrow;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 8 && row < kXRows; ++c) {
         const uint4 v = lds128(base + ((c ^ (row & 7)) << 4));
         const float2 f0 = unpack_f16x2(v.x), f1 = unpack_f16x2(v.y), f2 = unpack_f16x2(v.z), f3 = unpack_f16x2(v.w);
         acc[8 * c + 0] += f0.x;
@@ -728,19 +738,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kCacheFp8>::kT
 
 }  // namespace
 
-size_t decode_smem_bytes(int cache_dtype) { return cache_dtype ? smem_bytes<1>() : smem_bytes<0>(); }
+size_t decode_smem_bytes(int variant) {
+  return variant == 1 ? smem_bytes<1>() : (variant == 2 ? smem_bytes<2>() : smem_bytes<0>());
+}
 
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
-                          int cache_dtype, const DecodeArgs& a, int num_clusters, cudaStream_t s) {
-  const size_t smem = decode_smem_bytes(cache_dtype);
-  auto kern = cache_dtype ? decode_kernel<1> : decode_kernel<0>;
+                          int cache_dtype, int small_rows, const DecodeArgs& a, int num_clusters, cudaStream_t s) {
+  const int variant = cache_dtype ? 1 : (small_rows ? 2 : 0);
+  const size_t smem = decode_smem_bytes(variant);
+  auto kern = variant == 1 ? decode_kernel<1> : (variant == 2 ? decode_kernel<2> : decode_kernel<0>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the prologue (barriers, TMEM, cluster
   // sync) overlaps the plan kernel; the kernel waits for it before reading the plan
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
-  cfg.blockDim = dim3(cache_dtype ? Roles<1>::kThreads : Roles<0>::kThreads);
+  cfg.blockDim = dim3(variant == 1 ? Roles<1>::kThreads : Roles<0>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -3,7 +3,9 @@
 // CUDA graph).
 //
 // Query rows of a request are flattened as t*N + h and cut into groups of up
-// to 128 rows (the tcgen05 M of the decode kernel).  Every group reads the
+// to 128 rows (the tcgen05 M of the decode kernel; 32 for its small-rows
+// variant, used when every request has one query token and N <= 32, where
+// a group count never exceeds the batch size).  Every group reads the
 // keys its last row may see, L = seq_len - Sq + 1 + t (multi-token causal
 // rule of the AITER MLA backend's verify path), in 64-key tiles.  Groups are
 // laid end to end on one flattened tile axis which is either
@@ -54,7 +56,7 @@ __device__ int block_excl_scan(int v, int* total) {
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ qsl, int batch, int N,
                                                     int max_pages, int page_size, int num_splits, int C,
-                                                    Plan P) {
+                                                    int GR, Plan P) {
   __shared__ int s_flags;
   const int tid = threadIdx.x;
   if (tid == 0) s_flags = 0;
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (b < batch) {
       sq = qsl ? qsl[b + 1] - qsl[b] : 1;
       if (sq < 0) sq = 0;
-      ng = (int)(((long long)sq * N + kRows - 1) / kRows);
+      ng = (int)(((long long)sq * N + GR - 1) / GR);
     }
     int total;
     const int gb = block_excl_scan(ng, &total) + carry;
@@ -84,9 +86,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       for (int g = 0; g < ng && gb + g < P.max_groups; ++g) {
         GroupRec r;
         r.b = b;
-        r.row0 = q0 * N + g * kRows;
-        r.nrows = min(kRows, rows_b - g * kRows);
-        const int t_last = (g * kRows + r.nrows - 1) / N;
+        r.row0 = q0 * N + g * GR;
+        r.nrows = min(GR, rows_b - g * GR);
+        const int t_last = (g * GR + r.nrows - 1) / N;
         long long L = seq - sq + 1 + t_last;
         if (L < 0) L = 0;
         if (L > kv_cap) L = kv_cap;
@@ -199,9 +201,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
-                        int page_size, int num_splits, int num_clusters, Plan plan, cudaStream_t s) {
+                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s) {
   plan_kernel<<<1, 1024, 0, s>>>(seq_lens, qsl, batch, num_heads, max_pages, page_size, num_splits,
-                                 num_clusters, plan);
+                                 num_clusters, group_rows, plan);
   return cudaGetLastError();
 }
 
