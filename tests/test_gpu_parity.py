@@ -123,6 +123,23 @@ def test_decode_fp8_cache(num_heads, sq, page_size, num_splits):
     assert mla.decode_status(g.workspace) == 0
 
 
+@pytest.mark.parametrize("num_heads,sq,num_splits", [
+    (16, [1] * 8, 0), (32, [2, 0, 1, 1, 2, 0, 1, 1], 0), (24, [3, 0, 0, 1, 1, 1, 1, 1], 2), (20, [1] * 8, 3),
+])
+def test_decode_small_head_count(num_heads, sq, num_splits):
+    """Small head counts with as many query tokens as requests run the
+    small-rows kernel variant (32-row groups); requests with several tokens
+    span several groups there."""
+    batch = len(sq)
+    assert sum(sq) == batch
+    case = synth.make_decode_case(num_heads=num_heads, batch=batch, ctx=(60, 900), sq=sq, page_size=64,
+                                  seed=300 + num_heads + num_splits)
+    g = GpuCase(case, num_splits_max=num_splits)
+    g.decode(num_splits)
+    compare(case, g)
+    assert mla.decode_status(g.workspace) == 0
+
+
 def test_decode_edge_lengths():
     """seq_len 0 (padding request), Sq > seq_len, one-token contexts, exact
     multiples of the tile, lengths one past a tile."""
