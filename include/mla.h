@@ -129,7 +129,8 @@ MLA_API size_t mla_decode_workspace_size(int batch, int total_q, int num_heads, 
  *                    (query_start_loc[0] = 0, [batch] = total_q), or NULL for
  *                    one query token per request (then total_q == batch)
  *   num_heads        1..1024
- *   scale            softmax scale, passed explicitly (1/sqrt(P+R) for MLA)
+ *   scale            softmax scale, passed explicitly (1/sqrt(P+R) for MLA);
+ *                    finite and nonzero
  *   num_splits       0: split long contexts automatically to balance all SMs;
  *                    k > 0: cut every (request, 128-row group) into
  *                    min(k, tiles) contiguous pieces of near-equal length

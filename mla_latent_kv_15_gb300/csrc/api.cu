@@ -125,7 +125,7 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
     return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
   if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
     return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
-  if (!std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite");
+  if (!std::isfinite(scale) || scale == 0.f) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and nonzero");
   if (num_splits < 0 || num_splits > 4096) return fail(MLA_ERR_INVALID_ARG, "num_splits must be in [0, 4096]");
 
   const mla::WorkspaceLayout L = mla::workspace_layout(batch, total_q, num_heads, num_splits);
@@ -163,7 +163,9 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   a.total_rows = (int)rows;
   // an e4m3 row holds value / kv_scale: the scale folds into the scores and the output
   const float kvs = cache_dtype == MLA_FP8_E4M3 ? kv_scale : 1.f;
-  a.scale_log2 = scale * 1.4426950408889634f * kvs;
+  // the kernel works with a positive scale; a negative one negates q instead
+  a.scale_log2 = std::fabs(scale) * 1.4426950408889634f * kvs;
+  a.neg_q = scale < 0.f;
   a.out_scale = kvs;
   a.out = out;
   a.lse = lse;

@@ -112,7 +112,8 @@ struct DecodeArgs {
   int page_size;
   int num_blocks;
   int total_rows;           // total_q * num_heads: bound of every output row
-  float scale_log2;         // scale * log2(e) (* kv_scale for fp8)
+  float scale_log2;         // |scale| * log2(e) (* kv_scale for fp8), > 0
+  int neg_q;                // scale < 0: the kernel negates the query instead
   float out_scale;          // kv_scale for fp8, 1 for bf16
   void* out;                // bf16 [T*N, 512]
   float* lse;               // [T*N] or null

@@ -70,7 +70,6 @@ struct Layout {
   static constexpr int kXBytes = kXRows * kTile * 2;              // one fp16 partial score tile
 };
 constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
-constexpr int kSmallRows = 32;                    // unit rows of variant 2
 // Warp roles.
 //  bf16 cache (224 threads): 0 TMA producer, 1 score-MMA issuer (and TMEM
 //    owner), 2 P.V-MMA issuer, 3-6 softmax.
@@ -554,13 +553,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
 #pragma unroll
         for (int p = 0; p < kBoxesPerStage; ++p) {
           uint32_t q[32];
+          const uint32_t sgn = a.neg_q ? 0x80008000u : 0u;   // a negative scale negates q
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = lds128(base + p * kBox + ((c ^ (k & 7)) << 4));
-            q[4 * c + 0] = v.x;
-            q[4 * c + 1] = v.y;
-            q[4 * c + 2] = v.z;
-            q[4 * c + 3] = v.w;
+            q[4 * c + 0] = v.x ^ sgn;
+            q[4 * c + 1] = v.y ^ sgn;
+            q[4 * c + 2] = v.z ^ sgn;
+            q[4 * c + 3] = v.w ^ sgn;
           }
           if (rank == 0 && p == 4) {
             uint32_t h[16];
@@ -604,21 +604,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         }
         recv_s(it, cur, nbytes);
 
-        // scale (and mask on ragged tiles), tree max
+        // mask on ragged tiles, tree max of the unscaled scores (the scale is
+        // positive), then exp2(scale * s - m) as one FMA into the exponential
         const int key0 = (ur.tile_begin + jj) * kTile;
         if (key0 + kTile > lmin_warp) {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] * a.scale_log2 : -INFINITY;
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTile; ++c) cur[c] *= a.scale_log2;
+          for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
         }
         float mx[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(cur[c], cur[c + 16]), fmaxf(cur[c + 32], cur[c + 48]));
 #pragma unroll
         for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(mx[c], mx[c + 4]), fmaxf(mx[c + 8], mx[c + 12]));
-        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
         float alpha = 1.f;
         if (tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
@@ -630,8 +628,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kTile / 2; ++c) {
-          const float p0 = fast_exp2(cur[2 * c] - mref);
-          const float p1 = fast_exp2(cur[2 * c + 1] - mref);
+          const float p0 = fast_exp2(fmaf(cur[2 * c], a.scale_log2, -mref));
+          const float p1 = fast_exp2(fmaf(cur[2 * c + 1], a.scale_log2, -mref));
           ls[c & 3] += p0 + p1;
           pk[c] = pack_bf16x2(p0, p1);
         }

@@ -65,6 +65,10 @@ def test_host_validation_rejects_before_launch(lib):
     rc = lib.mla_decode(fake, fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 2, 16, 0.1, 0, fake, None,
                         P(1 << 24), 16, None)
     assert rc == -4
+    # zero softmax scale
+    rc = lib.mla_decode(fake, fake, fake, 10, 64, 0, 1.0, fake, 4, fake, 2, None, 2, 16, 0.0, 0, fake, None,
+                        fake, 1 << 30, None)
+    assert rc == -1 and b"scale" in lib.mla_last_error()
     # fp8 with a bad scale
     rc = lib.mla_cache_write(fake, fake, fake, 4, fake, 10, 64, 1, 0.0, None)
     assert rc == -1 and b"kv_scale" in lib.mla_last_error()

@@ -140,6 +140,16 @@ def test_decode_small_head_count(num_heads, sq, num_splits):
     assert mla.decode_status(g.workspace) == 0
 
 
+def test_decode_negative_scale():
+    """A negative softmax scale (the kernel negates q and works with |scale|)."""
+    case = synth.make_decode_case(num_heads=16, batch=4, ctx=(60, 500), page_size=64, seed=45)
+    case.scale = -case.scale
+    g = GpuCase(case)
+    g.decode()
+    compare(case, g)
+    assert mla.decode_status(g.workspace) == 0
+
+
 def test_decode_edge_lengths():
     """seq_len 0 (padding request), Sq > seq_len, one-token contexts, exact
     multiples of the tile, lengths one past a tile."""
