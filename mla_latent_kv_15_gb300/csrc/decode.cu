@@ -165,6 +165,13 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// three-input max (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -611,12 +618,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
 #pragma unroll
           for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
         }
-        float mx[16];
+        float mx[22];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(cur[c], cur[c + 16]), fmaxf(cur[c + 32], cur[c + 48]));
+        for (int c = 0; c < 21; ++c) mx[c] = fmax3(cur[3 * c], cur[3 * c + 1], cur[3 * c + 2]);
+        mx[21] = cur[63];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(mx[c], mx[c + 4]), fmaxf(mx[c + 8], mx[c + 12]));
-        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+        for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
+        mx[7] = mx[21];
+        const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) *
+                           a.scale_log2;
         float alpha = 1.f;
         if (tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
