@@ -172,6 +172,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// packed pair arithmetic (one f32x2 instruction for two fp32 lanes)
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n .reg .b64 x, y;\n mov.b64 x, {%0, %1};\n mov.b64 y, {%2, %3};\n add.rn.f32x2 x, x, y;\n"
+      " mov.b64 {%0, %1}, x;\n}" : "+f"(a0), "+f"(a1) : "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b, float c) {
+  asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %4};\n mov.b64 z, {%5, %5};\n"
+      " fma.rn.f32x2 x, x, y, z;\n mov.b64 {%0, %1}, x;\n}" : "=f"(r0), "=f"(r1) : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -515,14 +525,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       for (int c = 0; c < 8 && row < kXRows; ++c) {
         const uint4 v = lds128(base + ((c ^ (row & 7)) << 4));
         const float2 f0 = unpack_f16x2(v.x), f1 = unpack_f16x2(v.y), f2 = unpack_f16x2(v.z), f3 = unpack_f16x2(v.w);
-        acc[8 * c + 0] += f0.x;
-        acc[8 * c + 1] += f0.y;
-        acc[8 * c + 2] += f1.x;
-        acc[8 * c + 3] += f1.y;
-        acc[8 * c + 4] += f2.x;
-        acc[8 * c + 5] += f2.y;
-        acc[8 * c + 6] += f3.x;
-        acc[8 * c + 7] += f3.y;
+        add2(acc[8 * c + 0], acc[8 * c + 1], f0.x, f0.y);
+        add2(acc[8 * c + 2], acc[8 * c + 3], f1.x, f1.y);
+        add2(acc[8 * c + 4], acc[8 * c + 5], f2.x, f2.y);
+        add2(acc[8 * c + 6], acc[8 * c + 7], f3.x, f3.y);
       }
       // every row of buffer b is read before any thread sends its row of a
       // later tile: a received tile then proves the peer is done with the
@@ -638,9 +644,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kTile / 2; ++c) {
-          const float p0 = fast_exp2(fmaf(cur[2 * c], a.scale_log2, -mref));
-          const float p1 = fast_exp2(fmaf(cur[2 * c + 1], a.scale_log2, -mref));
-          ls[c & 3] += p0 + p1;
+          float x0, x1;
+          fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, -mref);
+          const float p0 = fast_exp2(x0);
+          const float p1 = fast_exp2(x1);
+          add2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], p0, p1);
           pk[c] = pack_bf16x2(p0, p1);
         }
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
