@@ -58,14 +58,15 @@ constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 c
 constexpr int kStageBytes = kBoxesPerStage * kBox;
 constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
 constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
-constexpr int kFp8Slots = 2;                      // e4m3 staging ring (two tiles in flight)
-// Kernel variants: 0 bf16 cache; 1 e4m3 cache; 2 bf16 cache with at most 32
+// An e4m3 tile lands in the upper half of the bf16 stage it is expanded into.
+constexpr int kFp8InPlace = kStageBytes - kFp8TileBytes;
+// Kernel variants: 0 bf16 cache; 1 e4m3 cache (expanded in place in the bf16
+// ring); 2 bf16 cache with at most 32
 // query rows per unit (small head counts: the receive ring shrinks to 32-row
 // buffers and the cache ring gets a fifth stage).
 template <int kVariant>
 struct Layout {
-  static constexpr int kStages = kVariant == 1 ? 3 : (kVariant == 2 ? 5 : 4);
-  static constexpr int kStagingBytes = kVariant == 1 ? kFp8Slots * kFp8TileBytes : 0;
+  static constexpr int kStages = kVariant == 2 ? 5 : 4;
   static constexpr int kXRows = kVariant == 2 ? 32 : kRows;        // rows of a receive buffer
   static constexpr int kXBytes = kXRows * kTile * 2;              // one fp16 partial score tile
 };
@@ -85,9 +86,9 @@ struct Roles {
   static constexpr int kPV = kCacheFp8 ? 10 : 2;
 };
 constexpr int kWarpExpand0 = 4;   // e4m3 cache only
-// e4m3 registers per thread after the split (launch: 168): 128 x (248 + 88 +
-// 112) = 57344 stay within the 384 x 168 the CTA is launched with.
-constexpr uint32_t kRegsSoftmax = 248, kRegsExpand = 88, kRegsIssue = 112;
+// e4m3 registers per thread after the split (launch: 168): 128 x (248 + 120 +
+// 112) = 61440 stay within the 384 x 168 the CTA is launched with.
+constexpr uint32_t kRegsSoftmax = 248, kRegsExpand = 120, kRegsIssue = 112;
 static_assert(128 * (kRegsSoftmax + kRegsExpand + kRegsIssue) <= 384 * 168, "register split");
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
 
@@ -104,8 +105,7 @@ constexpr int kMaxStages = 5;
 struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];  // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
-  uint64_t stg_full[kFp8Slots];   // e4m3 tile landed in the staging ring
-  uint64_t stg_empty[kFp8Slots];  // the expansion warps are done with a staging slot
+  uint64_t stg_full[kMaxStages];  // e4m3 tile landed in the upper half of its ring slot
   uint64_t q_ready;
   uint64_t s_full;
   uint64_t s_free;
@@ -121,7 +121,7 @@ struct __align__(8) Barriers {
 
 template <int kVariant>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Layout<kVariant>::kStages * kStageBytes + Layout<kVariant>::kStagingBytes +
+  return 1024 + (size_t)Layout<kVariant>::kStages * kStageBytes +
          kXBuffers * (size_t)Layout<kVariant>::kXBytes + sizeof(Barriers);
 }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
@@ -205,29 +205,38 @@ __device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
   return rank == 0 ? (p < 4 || k < 2) : (p > 0 || k >= 2);
 }
 
-// Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major) into the bf16
-// 128-byte-swizzled layout the MMAs read (what a bf16 TMA load would have
-// written).  e4m3 -> f16 -> f32 -> bf16 is exact: every e4m3 value is a bf16
-// value.  Runs on the 128 threads of the expansion warps.
-__device__ __forceinline__ void expand_e4m3_tile(uint32_t src, uint32_t dst, int t) {
-#pragma unroll 2
-  for (int i = t; i < kBoxesPerStage * 64 * 4; i += 128) {
-    const int q = i & 3;               // 16-value chunk inside the 64-value row
-    const int r = (i >> 2) & 63;       // row (key)
-    const int p = i >> 8;              // box
-    const uint4 v = lds128(src + p * kFp8Box + r * 64 + q * 16);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major, in the upper
+// half of the ring slot) into the bf16 128-byte-swizzled layout the MMAs read
+// (what a bf16 TMA load would have written), in place: every thread first
+// reads its share of the whole tile, then all write.  e4m3 -> f16 -> f32 ->
+// bf16 is exact: every e4m3 value is a bf16 value.  Runs on the 128 threads of
+// the expansion warps.
+__device__ __forceinline__ void expand_e4m3_tile(uint32_t stage, int t) {
+  constexpr int kPer = kBoxesPerStage * 64 * 4 / 128;    // 16-value chunks per thread
+  uint4 v[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 128 * k;
+    const int q = i & 3, r = (i >> 2) & 63, p = i >> 8;   // chunk in the row, row (key), box
+    v[k] = lds128(stage + kFp8InPlace + p * kFp8Box + r * 64 + q * 16);
+  }
+  named_bar_expand();
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = t + 128 * k;
+    const int q = i & 3, r = (i >> 2) & 63, p = i >> 8;
+    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
     uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] & 0xFFFF), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[k] >> 16), __NV_E4M3);
+    for (int j = 0; j < 4; ++j) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] & 0xFFFF), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] >> 16), __NV_E4M3);
       const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
       const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      o[2 * k] = pack_bf16x2(flo.x, flo.y);
-      o[2 * k + 1] = pack_bf16x2(fhi.x, fhi.y);
+      o[2 * j] = pack_bf16x2(flo.x, flo.y);
+      o[2 * j + 1] = pack_bf16x2(fhi.x, fhi.y);
     }
-    const uint32_t row = dst + p * kBox + r * 128;
+    const uint32_t row = stage + p * kBox + r * 128;
     sts128(row + (((2 * q) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
     sts128(row + (((2 * q + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
   }
@@ -244,8 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
-  uint8_t* staging = stages + kStages * kStageBytes;     // e4m3 tiles (fp8 cache only)
-  uint8_t* x_recv = staging + Layout<kVariant>::kStagingBytes;   // receive ring
+  uint8_t* x_recv = stages + kStages * kStageBytes;      // receive ring
   Barriers* bars = reinterpret_cast<Barriers*>(x_recv + kXBuffers * kXBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -260,10 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       mbar_init(smem_u32(&bars->kv_full[i]), 1);
       mbar_init(smem_u32(&bars->kv_empty[i]), 2);
     }
-    for (int i = 0; i < kFp8Slots; ++i) {
-      mbar_init(smem_u32(&bars->stg_full[i]), 1);
-      mbar_init(smem_u32(&bars->stg_empty[i]), 1);
-    }
+    for (int i = 0; i < kMaxStages; ++i) mbar_init(smem_u32(&bars->stg_full[i]), 1);
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), 4);
@@ -302,11 +307,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
   auto producer = [&]() {
     // ------------------------------------------------------------ producer
     // Lane 0 streams everything with TMA: bf16 tiles straight into the ring;
-    // e4m3 tiles into the staging ring, which the expansion warps turn into
+    // e4m3 tiles into the upper half of the ring slot, which the expansion warps turn into
     // the bf16 ring slots the MMAs read.
     const bool leader = lane == 0;
     if (leader) {
-      uint32_t item = 0, g = 0;
+      uint32_t item = 0;
       const int sub_rows = a.page_size < kTile ? a.page_size : kTile;
       const int nsub = kTile / sub_rows;
       const int oob_row = a.num_blocks * a.page_size;  // first row past the cache: reads zeros
@@ -348,6 +353,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
             else
               tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
           }
+          // e4m3 cache: a query item also completes a phase of the slot's
+          // stg_full, so its phases count every item of the slot
+          if (kCacheFp8) mbar_arrive(smem_u32(&bars->stg_full[slot]));
         }
         for (int jj = 0; jj < ntiles; ++jj, ++item) {
           const uint32_t slot = item % kStages, round = item / kStages;
@@ -357,12 +365,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
             mbar_expect_tx(full, kStageBytes);
             load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full, 128);
           } else {
-            const uint32_t sl = g % kFp8Slots;
-            wait_bar(ctx, &bars->stg_empty[sl], ((g / kFp8Slots) & 1) ^ 1);
-            const uint32_t full = smem_u32(&bars->stg_full[sl]);
+            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+            const uint32_t full = smem_u32(&bars->stg_full[slot]);
             mbar_expect_tx(full, kFp8TileBytes);
-            load_tile(ur.tile_begin + jj, smem_u32(staging + sl * kFp8TileBytes), full, 64);
-            ++g;
+            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kFp8InPlace), full, 64);
           }
         }
       }
@@ -447,22 +453,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
   auto expander = [&]() {
     // -------------------------------------------------------- e4m3 expansion
     const int te = threadIdx.x - 32 * kWarpExpand0;
-    uint32_t item = 0, g = 0;
+    uint32_t item = 0;
     for (int u = ubeg; u < uend; ++u) {
       const UnitRec ur = P.units[u];
       const int ntiles = ur.tile_end - ur.tile_begin;
       item += 2;  // the query items are loaded by the producer
-      for (int jj = 0; jj < ntiles; ++jj, ++item, ++g) {
+      for (int jj = 0; jj < ntiles; ++jj, ++item) {
         const uint32_t slot = item % kStages, round = item / kStages;
-        const uint32_t sl = g % kFp8Slots;
-        wait_bar(ctx, &bars->stg_full[sl], (g / kFp8Slots) & 1);
-        wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
-        expand_e4m3_tile(smem_u32(staging + sl * kFp8TileBytes), smem_u32(stages + slot * kStageBytes), te);
-        fence_proxy_async_smem();    // bf16 writes visible to the MMAs; staging reads done before reuse
+        wait_bar(ctx, &bars->stg_full[slot], round & 1);
+        expand_e4m3_tile(smem_u32(stages + slot * kStageBytes), te);
+        fence_proxy_async_smem();    // bf16 writes visible to the MMAs
         named_bar_expand();
         if (te == 0) {
           mbar_arrive(smem_u32(&bars->kv_full[slot]));
-          mbar_arrive(smem_u32(&bars->stg_empty[sl]));
         }
       }
     }
