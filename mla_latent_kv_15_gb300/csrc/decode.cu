@@ -160,6 +160,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// 32-byte global store (one whole sector); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                             uint32_t f, uint32_t g, uint32_t h) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+               "r"(e), "r"(f), "r"(g), "r"(h)
+               : "memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -481,6 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // 32-byte stores allowed
     int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
     // Load partial scores of tile `t` from TMEM into `dst` and free the S columns.
@@ -691,23 +700,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         tmem_wait_ld();
         if (!valid) continue;
         const int d0 = 256 * rank + 32 * ch;
+        // whole 32-byte sectors per store where the address allows (a row is
+        // one thread's: 16-byte stores would write half sectors)
         if (ur.slot < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0);
+          uint32_t w[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = w;
+          for (int v = 0; v < 16; ++v)
+            w[v] = pack_bf16x2(__uint_as_float(o[2 * v]) * inv, __uint_as_float(o[2 * v + 1]) * inv);
+          __nv_bfloat16* dst = out + (size_t)R * kLkv + d0;
+          if (out32) {
+            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(P.part_o + ((size_t)ur.slot * kRows + row) * kLkv + d0);
+          float* dst = P.part_o + ((size_t)ur.slot * kRows + row) * kLkv + d0;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          for (int v = 0; v < 4; ++v)
+            st_global_v8(dst + 8 * v, __float_as_uint(__uint_as_float(o[8 * v]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 1]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 2]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 3]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 4]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 5]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 6]) * inv),
+                         __float_as_uint(__uint_as_float(o[8 * v + 7]) * inv));
         }
       }
       if (valid && rank == 0) {
