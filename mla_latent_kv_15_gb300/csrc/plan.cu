@@ -59,6 +59,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     int GR, Plan P) {
   __shared__ int s_flags;
   const int tid = threadIdx.x;
+  // Launched as a programmatic dependent of the kernel before it on the
+  // stream, so only its launch overlaps that kernel's tail: it waits for that
+  // grid (which may have written seq_lens or query_start_loc, or still read
+  // an earlier plan) before touching memory. The decode kernel waits only for
+  // this grid, which therefore also orders it after everything earlier.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) s_flags = 0;
   __syncthreads();
   const long long kv_cap = (long long)max_pages * page_size;
@@ -202,8 +208,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, qsl, batch, num_heads, max_pages, page_size, num_splits,
-                                 num_clusters, group_rows, plan);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, qsl, batch, num_heads, max_pages, page_size,
+                                     num_splits, num_clusters, group_rows, plan);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
