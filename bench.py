@@ -7,7 +7,10 @@ Default workload: DeepSeek-V3-shaped decode, N=128 heads, batch 64, contexts
 uniform in [1024, 8192], page 64, bf16 cache in a 40k-page pool.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                       [--workload NAME]
+                       [--workload NAME] [--op decode|q_absorb|v_up_proj]
+--op q_absorb / v_up_proj times the per-head projections around the decode
+(query absorption q_nope @ W_UK_T, value up-projection o_latent @ W_UV) on
+the workload's token and head counts instead of the decode step.
 Prints one JSON line.  With --gpus N > 1 (under torchrun) every rank runs an
 independent replica (the decode of one batch does not shard), value = tokens of
 all ranks / max time over ranks.  --impl reference times the fp64 CPU oracle
@@ -402,6 +405,111 @@ def run_reference(args):
     }
 
 
+def run_proj(args):
+    """One per-head projection per step (random bf16 weights of the
+    DeepSeek-V3 shapes: P = V = 128, Lkv = 512), L2 flushed before every
+    launch (the weights alone would fit in L2)."""
+    import torch
+    import mla_latent_kv_15_gb300 as mla
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    mla.load()
+    cfg = synth.WORKLOADS[args.workload]
+    N = cfg["num_heads"]
+    sq = cfg["sq"]
+    T = sum(sq) if isinstance(sq, list) else cfg["batch"] * sq
+    P = V = 128
+    dev = "cuda"
+    w_uk, w_uv = synth.projection_weights(0, N, p=P, v=V)
+    if args.op == "q_absorb":
+        d_in, d_out, stride = P, synth.LKV, P + synth.ROPE     # q_nope = the first 128 columns of q
+        w_host = np.ascontiguousarray(w_uk.transpose(1, 2, 0))   # (N, P, L)
+    else:
+        d_in, d_out, stride = synth.LKV, V, synth.LKV
+        w_host = np.ascontiguousarray(w_uv.transpose(1, 0, 2))   # (N, L, V)
+    x_bits = synth.bf16_normal(1, (T, N, stride))
+
+    def t16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    w = t16(w_host).to(dev)
+    x_h = t16(x_bits).pin_memory()
+    x = x_h.to(dev)
+    y = torch.empty((T, N, d_out), dtype=torch.bfloat16, device=dev)
+    y_h = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+
+    def op(xx, yy):
+        if args.op == "q_absorb":
+            mla.q_absorb(xx[:, :, :P], w, yy)
+        else:
+            mla.v_up_proj(xx, w, yy)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        op(x, y)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    with sampler:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            op(x, y)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if mla.proj_status() != 0:
+        raise RuntimeError("projection kernel reported a device error")
+    # e2e through the public API: x in from pinned host memory, y back
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        x.copy_(x_h, non_blocking=True)
+        op(x, y)
+        y_h.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    alg_bytes = T * N * d_in * 2 + N * d_in * d_out * 2 + T * N * d_out * 2
+    flops = 2 * T * N * d_in * d_out
+    hbm, _, src = peaks()
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    res = {
+        "metric": f"{args.op} tokens/s + HBM GB/s & % roofline (N={N}, T={T}, {d_in}->{d_out} per head)",
+        "op": args.op, "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload} token/head counts", "num_heads": N, "num_tokens": T,
+                   "d_in": d_in, "d_out": d_out, "x_row_stride": stride,
+                   "l2": "flushed (256 MiB write) before every timed launch",
+                   "timing": "CUDA events around each launch on the launching stream"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": alg_bytes, "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": round(T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.numel() * 2, "d2h_bytes_per_step": y_h.numel() * 2,
+                "copies": "pinned host buffers, copies and launch serialised on one stream"},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        from oracle import expanded
+        import oracle
+        xf = oracle.bf16_to_f64(x_bits[:, :, :d_in])
+        t0 = time.perf_counter()
+        if args.op == "q_absorb":
+            expanded.absorb_query(xf, oracle.bf16_to_f64(w_uk))
+        else:
+            expanded.up_project(xf, oracle.bf16_to_f64(w_uv))
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(T / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                               "sample": f"the whole op ({T} tokens x {N} heads), numpy einsum in fp64, {el:.2f} s"}
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,10 +521,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "q_absorb", "v_up_proj"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.op != "decode" and args.impl == "ours":
+        res = run_proj(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -217,6 +217,64 @@ MLA_API int mla_decode_no_alloc(const void* q_abs, const void* q_pe, const void*
                                 const int32_t* query_start_loc, int total_q, int num_heads, float scale,
                                 int num_splits, void* out, float* lse, void* stream);
 
+/*
+ * mla_q_absorb -- query absorption of the decode branch (common.py,
+ * MLACommonImpl.forward: "Multiply (N, B, P) x (N, P, L) -> (N, B, L)",
+ * torch.bmm(decode_q_nope, self.W_UK_T); the docstring's
+ * ql_nope = einsum("snp,lnp->snl", q_nope, W_UK)):
+ *
+ *   ql_nope[t, n, l] = sum_p q_nope[t, n, p] * w_uk_t[n, p, l]
+ *
+ * written as [num_tokens, num_heads, 512] bf16, the q_abs layout mla_decode
+ * reads.  Products accumulate in float32 on the tensor cores; the result is
+ * rounded to bf16 (nearest even).
+ *   q_nope        bf16, row (t, n) at q_nope + (t * num_heads + n) * q_row_stride
+ *                 elements; q_row_stride >= nope_dim and a multiple of 8 (192
+ *                 reads the first 128 columns of q = [q_nope | q_pe]);
+ *                 16-byte aligned
+ *   w_uk_t        [num_heads, nope_dim, 512] bf16, dense (W_UK_T in the (N, P, L)
+ *                 order process_weights_after_loading stores), 16-byte aligned
+ *   ql_nope       [num_tokens, num_heads, 512] bf16, dense, 16-byte aligned;
+ *                 must not overlap q_nope
+ *   nope_dim      multiple of 64 in [64, 1024] (DeepSeek-V3: 128)
+ *   num_heads     [1, 1024]; num_tokens in [0, 8388480]; 0 is a no-op.
+ * One launch (a programmatic dependent of the previous kernel on `stream`).
+ * Device-side timeouts set MLA_DEVERR_TIMEOUT in the word mla_proj_status reads.
+ */
+MLA_API int mla_q_absorb(const void* q_nope, int64_t q_row_stride, const void* w_uk_t, int64_t num_tokens,
+                         int num_heads, int nope_dim, void* ql_nope, void* stream);
+
+/*
+ * mla_v_up_proj -- the value up-projection after the latent decode (common.py,
+ * MLACommonBaseImpl._v_up_proj: "Multiply (N, B, L) x (N, L, V) -> (N, B, V)",
+ * torch.bmm(x, self.W_UV); the docstring's einsum("snl,lnv->snv", o, W_UV)):
+ *
+ *   out[t, n, v] = sum_l o_lat[t, n, l] * w_uv[n, l, v]
+ *
+ * written as [num_tokens, num_heads, v_head_dim] bf16 (= the [T, N * V] input
+ * of the output projection).  float32 accumulation, bf16 result (nearest even).
+ *   o_lat         [num_tokens, num_heads, 512] bf16, dense (mla_decode's out),
+ *                 16-byte aligned
+ *   w_uv          [num_heads, 512, v_head_dim] bf16, dense (W_UV in the (N, L, V)
+ *                 order process_weights_after_loading stores), 16-byte aligned
+ *   out           [num_tokens, num_heads, v_head_dim] bf16, dense, 16-byte
+ *                 aligned; must not overlap o_lat
+ *   v_head_dim    multiple of 64 in [64, 256], or 512 or 1024 (DeepSeek-V3: 128)
+ *   num_heads     [1, 1024]; num_tokens in [0, 8388480]; 0 is a no-op.
+ * One launch, as for mla_q_absorb.
+ */
+MLA_API int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_tokens, int num_heads, int v_head_dim,
+                          void* out, void* stream);
+
+/*
+ * mla_proj_status -- copy the device error word of the projection kernels
+ * (mla_q_absorb, mla_v_up_proj; OR of mla_device_error bits, 0 = clean) to
+ * *status, then clear it if `clear` is non-zero.  The word is shared by every
+ * projection launched in the process on the current device.  Synchronises
+ * `stream`.
+ */
+MLA_API int mla_proj_status(int* status, int clear, void* stream);
+
 /* Human-readable description of the calling thread's last error ("" if none). */
 MLA_API const char* mla_last_error(void);
 

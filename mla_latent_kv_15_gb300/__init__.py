@@ -28,7 +28,7 @@ DQK = 576
 
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
-                 "mla_decode_no_alloc")
+                 "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -67,6 +67,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_set_decode_timing_events.argtypes = [P, P]
     lib.mla_decode_no_alloc.restype = i32
     lib.mla_decode_no_alloc.argtypes = [P, P, P, i64, i32, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P]
+    lib.mla_q_absorb.restype = i32
+    lib.mla_q_absorb.argtypes = [P, i64, P, i64, i32, i32, P, P]
+    lib.mla_v_up_proj.restype = i32
+    lib.mla_v_up_proj.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.mla_proj_status.restype = i32
+    lib.mla_proj_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
     _lib = lib
     return lib
 
@@ -148,6 +154,30 @@ def merge_states(o_a, lse_a, o_b, lse_b, out, lse_out=None, stream=None) -> None
     code = MLA_BF16 if o_a.dtype == torch.bfloat16 else MLA_FP32
     _check(load().mla_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, dim, code, _ptr(out),
                                    _ptr(lse_out), _stream(stream)))
+
+
+def q_absorb(q_nope, w_uk_t, ql_nope, stream=None) -> None:
+    """ql_nope[t, n, :] = q_nope[t, n, :] @ w_uk_t[n] (bf16; w_uk_t [N, P, 512]).
+    ``q_nope`` [T, N, P] may be a column slice of a wider tensor (for example
+    ``q[..., :128]`` of q = [q_nope | q_pe]): its last dimension must be
+    contiguous and the (t, n) rows equally spaced."""
+    T, N, P_ = q_nope.shape
+    if q_nope.stride(2) != 1 or q_nope.stride(0) != N * q_nope.stride(1):
+        raise ValueError("q_nope rows must be equally spaced with a contiguous last dimension")
+    _check(load().mla_q_absorb(_ptr(q_nope), q_nope.stride(1), _ptr(w_uk_t), T, N, P_, _ptr(ql_nope),
+                               _stream(stream)))
+
+
+def v_up_proj(o_lat, w_uv, out, stream=None) -> None:
+    """out[t, n, :] = o_lat[t, n, :] @ w_uv[n] (bf16; w_uv [N, 512, V], out [T, N, V])."""
+    T, N, _ = o_lat.shape
+    _check(load().mla_v_up_proj(_ptr(o_lat), _ptr(w_uv), T, N, w_uv.shape[2], _ptr(out), _stream(stream)))
+
+
+def proj_status(clear: bool = False, stream=None) -> int:
+    st = ctypes.c_int(0)
+    _check(load().mla_proj_status(ctypes.byref(st), int(clear), _stream(stream)))
+    return st.value
 
 
 def set_decode_timing_events(start=None, stop=None) -> None:

@@ -220,3 +220,66 @@ int mla_merge_states(const void* o_a, const float* lse_a, const void* o_b, const
 }
 
 }  // extern "C"
+
+namespace {
+
+// Shared body of the two per-head projections: validation of what both have
+// in common, tensor maps, launch.
+int head_proj(const char* name, const void* x, int64_t x_stride, const void* w, int64_t T, int N, int d_in,
+              int d_out, void* y, void* stream) {
+  if (T < 0) return fail(MLA_ERR_INVALID_ARG, "%s: num_tokens must be >= 0", name);
+  if (T > 65535LL * 128) return fail(MLA_ERR_UNSUPPORTED, "%s: num_tokens must be <= 8388480", name);
+  if (N < 1 || N > 1024) return fail(MLA_ERR_INVALID_ARG, "%s: num_heads must be in [1, 1024]", name);
+  if (T == 0) return ok();
+  if (!x || !w || !y) return fail(MLA_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16))
+    return fail(MLA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", name);
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x), yb = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t xe = xb + (uintptr_t)((T * N - 1) * x_stride + d_in) * 2, ye = yb + (uintptr_t)(T * N * d_out) * 2;
+  if (xb < ye && yb < xe) return fail(MLA_ERR_INVALID_ARG, "%s: the output must not overlap the input", name);
+  CUtensorMap tm_x, tm_w;
+  if (!mla::encode_tmap_3d(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)d_in, (uint64_t)N, (uint64_t)T,
+                           (uint64_t)x_stride * 2, (uint64_t)x_stride * 2 * N, 64, 1, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !mla::encode_tmap_2d(&tm_w, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)d_out, (uint64_t)N * d_in,
+                           (uint64_t)d_out * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(MLA_ERR_CUDA, "%s: tensor map encoding failed", name);
+  cudaError_t e = mla::launch_head_proj(tm_x, tm_w, y, T, N, d_in, d_out, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_q_absorb(const void* q_nope, int64_t q_row_stride, const void* w_uk_t, int64_t num_tokens, int num_heads,
+                 int nope_dim, void* ql_nope, void* stream) {
+  if (nope_dim < 64 || nope_dim > 1024 || nope_dim % 64 != 0)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_q_absorb: nope_dim must be a multiple of 64 in [64, 1024] (got %d)",
+                nope_dim);
+  if (q_row_stride < nope_dim || q_row_stride % 8 != 0 || q_row_stride > (1LL << 24))
+    return fail(MLA_ERR_INVALID_ARG, "mla_q_absorb: q_row_stride must be >= nope_dim, a multiple of 8 and <= 2^24");
+  return head_proj("mla_q_absorb", q_nope, q_row_stride, w_uk_t, num_tokens, num_heads, nope_dim, mla::kLkv,
+                   ql_nope, stream);
+}
+
+int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_tokens, int num_heads, int v_head_dim, void* out,
+                  void* stream) {
+  const bool ok_dim = (v_head_dim >= 64 && v_head_dim <= 256 && v_head_dim % 64 == 0) || v_head_dim == 512 ||
+                      v_head_dim == 1024;
+  if (!ok_dim)
+    return fail(MLA_ERR_UNSUPPORTED, "mla_v_up_proj: v_head_dim must be 64, 128, 192, 256, 512 or 1024 (got %d)",
+                v_head_dim);
+  return head_proj("mla_v_up_proj", o_lat, mla::kLkv, w_uv, num_tokens, num_heads, mla::kLkv, v_head_dim, out,
+                   stream);
+}
+
+int mla_proj_status(int* status, int clear, void* stream) {
+  if (!status) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  cudaError_t e = mla::head_proj_status(status, clear, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "projection status read");
+  return ok();
+}
+
+}  // extern "C"

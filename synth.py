@@ -235,3 +235,20 @@ def random_partials(seed: int, rows: int, dim: int = LKV, neg_inf_frac: float = 
         lse_a[rng.random(rows) < neg_inf_frac] = -np.inf
         lse_b[rng.random(rows) < neg_inf_frac] = -np.inf
     return o_a, lse_a, o_b, lse_b
+
+
+def projection_weights(seed: int, num_heads: int, lkv: int = LKV, p: int = 128, v: int = 128):
+    """bf16 bit patterns of W_UK [Lkv, N, P] and W_UV [Lkv, N, V] (the split of
+    kv_b_proj's transposed weight, common.py process_weights_after_loading),
+    drawn N(0, 1/Lkv) in float32 and rounded to bf16 (RNE)."""
+    rng = np.random.Generator(np.random.PCG64(30_000 + seed))
+    sd = np.float32(1.0 / math.sqrt(lkv))
+    w_uk = rng.standard_normal((lkv, num_heads, p), dtype=np.float32) * sd
+    w_uv = rng.standard_normal((lkv, num_heads, v), dtype=np.float32) * sd
+    return to_bf16_bits(w_uk), to_bf16_bits(w_uv)
+
+
+def bf16_normal(seed: int, shape, std: float = 0.5) -> np.ndarray:
+    """bf16 bit patterns of N(0, std^2) float32 draws (RNE)."""
+    rng = np.random.Generator(np.random.PCG64(40_000 + seed))
+    return to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(std))

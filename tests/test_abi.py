@@ -84,6 +84,28 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.mla_last_error() == b""
 
 
+def test_projection_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    x, w, y = P(1 << 20), P(1 << 28), P(1 << 32)       # never dereferenced
+    # unsupported widths
+    assert lib.mla_v_up_proj(x, w, 4, 2, 96, y, None) == -2 and b"v_head_dim" in lib.mla_last_error()
+    assert lib.mla_q_absorb(x, 128, w, 4, 2, 100, y, None) == -2 and b"nope_dim" in lib.mla_last_error()
+    # row stride below the width or not a multiple of 8
+    assert lib.mla_q_absorb(x, 64, w, 4, 2, 128, y, None) == -1 and b"q_row_stride" in lib.mla_last_error()
+    assert lib.mla_q_absorb(x, 196, w, 4, 2, 128, y, None) == -1
+    # head count, misalignment, null pointers, overlap of input and output
+    assert lib.mla_v_up_proj(x, w, 4, 0, 128, y, None) == -1 and b"num_heads" in lib.mla_last_error()
+    assert lib.mla_v_up_proj(P((1 << 20) + 8), w, 4, 2, 128, y, None) == -1
+    assert lib.mla_v_up_proj(None, w, 4, 2, 128, y, None) == -1
+    assert lib.mla_v_up_proj(x, w, 4, 2, 128, P((1 << 20) + 64), None) == -1 and b"overlap" in lib.mla_last_error()
+    assert lib.mla_q_absorb(x, 192, w, -1, 2, 128, y, None) == -1
+    # empty batch is a no-op that touches nothing
+    assert lib.mla_v_up_proj(None, None, 0, 2, 128, None, None) == 0
+    assert lib.mla_q_absorb(None, 128, None, 0, 2, 128, None, None) == 0
+    assert lib.mla_last_error() == b""
+    assert lib.mla_proj_status(None, 0, None) == -1
+
+
 def test_product_fails_loudly_without_library(tmp_path):
     """No fallback: a missing library is an ImportError, not a CPU path."""
     import mla_latent_kv_15_gb300 as mla

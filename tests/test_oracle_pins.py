@@ -29,6 +29,30 @@ def _rows_in_order(case, b):
 
 # ------------------------------------------------------------ two-path identity
 
+def test_projections_select_with_one_hot_weights():
+    """A one-hot W_UV / W_UK picks one input column per output column, and
+    zero columns give zeros: pins which operand axis each einsum contracts."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    T, N, L, P, V = 3, 4, 512, 128, 64
+    o_lat = rng.standard_normal((T, N, L))
+    pick = rng.permutation(L)[:V]
+    w_uv = np.zeros((L, N, V))
+    for n in range(N):
+        w_uv[pick, n, np.arange(V)] = 1.0
+    w_uv[:, 2, :] = 0.0
+    o = expanded.up_project(o_lat, w_uv)
+    want = o_lat[:, :, pick].copy()
+    want[:, 2, :] = 0.0
+    assert np.array_equal(o, want)
+    q_nope = rng.standard_normal((T, N, P))
+    w_uk = np.zeros((L, N, P))
+    src = rng.integers(0, P, size=L)
+    for n in range(N):
+        w_uk[np.arange(L), n, src] = n + 1.0
+    ql = expanded.absorb_query(q_nope, w_uk)
+    assert np.array_equal(ql, q_nope[:, :, src] * (np.arange(N) + 1.0)[None, :, None])
+
+
 @pytest.mark.parametrize("sq", [1, 4])
 def test_two_path_identity(sq):
     """Absorbed MQA + W_UV up-projection == expanded MHA (common.py docstring,
