@@ -239,7 +239,8 @@ int head_proj(const char* name, const void* x, int64_t x_stride, const void* w, 
   if (xb < ye && yb < xe) return fail(MLA_ERR_INVALID_ARG, "%s: the output must not overlap the input", name);
   CUtensorMap tm_x, tm_w;
   if (!mla::encode_tmap_3d(&tm_x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)d_in, (uint64_t)N, (uint64_t)T,
-                           (uint64_t)x_stride * 2, (uint64_t)x_stride * 2 * N, 64, 1, 128,
+                           (uint64_t)x_stride * 2, (uint64_t)x_stride * 2 * N, 64, 1,
+                           (uint32_t)mla::head_proj_x_rows(T),
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !mla::encode_tmap_2d(&tm_w, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)d_out, (uint64_t)N * d_in,
                            (uint64_t)d_out * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -134,11 +134,12 @@ cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void*
 cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
                                void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s);
 size_t decode_smem_bytes(int variant);
-// y[t, n, :] = x[t, n, :] @ W[n] (tensor maps: x 3-D {d_in, N, T} boxes 64x1x128,
-// W 2-D {d_out, N*d_in} boxes 64x64, both 128-byte swizzled)
+// y[t, n, :] = x[t, n, :] @ W[n] (tensor maps: x 3-D {d_in, N, T} boxes
+// 64 x 1 x head_proj_x_rows(T), W 2-D {d_out, N*d_in} boxes 64x64, both
+// 128-byte swizzled)
 cudaError_t launch_head_proj(const CUtensorMap& tm_x, const CUtensorMap& tm_w, void* y, int64_t T, int N, int d_in,
                              int d_out, cudaStream_t s);
-size_t head_proj_smem_bytes(int d_in, int d_out);
+int head_proj_x_rows(int64_t T);
 cudaError_t head_proj_status(int* status, int clear, cudaStream_t s);
 
 }  // namespace mla
