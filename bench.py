@@ -531,6 +531,48 @@ def run_proj(args):
     return res
 
 
+def run_proj_reference(args):
+    """--impl reference --op ...: the oracle's fp64 einsum for the projection,
+    timed on the host over K steps of the same inputs as the GPU arm."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    import oracle
+    from oracle import expanded
+    cfg = synth.WORKLOADS[args.workload]
+    N = cfg["num_heads"]
+    sq = cfg["sq"]
+    T = sum(sq) if isinstance(sq, list) else cfg["batch"] * sq
+    P = V = 128
+    w_uk, w_uv = synth.projection_weights(0, N, p=P, v=V)
+    if args.op == "q_absorb":
+        d_in, d_out = P, synth.LKV
+        x = oracle.bf16_to_f64(synth.bf16_normal(1, (T, N, P + synth.ROPE))[:, :, :P])
+        w, f = oracle.bf16_to_f64(w_uk), expanded.absorb_query
+    else:
+        d_in, d_out = synth.LKV, V
+        x = oracle.bf16_to_f64(synth.bf16_normal(1, (T, N, synth.LKV)))
+        w, f = oracle.bf16_to_f64(w_uv), expanded.up_project
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        f(x, w)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    v = T / (ms * 1e-3)
+    return {
+        "metric": f"{args.op} tokens/s + HBM GB/s & % roofline (N={N}, T={T}, {d_in}->{d_out} per head)",
+        "op": args.op, "impl": "reference", "value": round(v, 3), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} token/head counts", "num_heads": N, "num_tokens": T,
+                   "d_in": d_in, "d_out": d_out},
+        "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the whole op per step, numpy einsum in fp64, {args.steps} steps"},
+        "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -546,8 +588,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.op != "decode" and args.impl == "ours":
-        res = run_proj(args)
+    if args.op != "decode":
+        res = run_proj_reference(args) if args.impl == "reference" else run_proj(args)
     else:
         res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
