@@ -64,6 +64,8 @@ def _load():
                                       P, i64, i64, i64, P, P, i32]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [P, P, P, P, i64, i32, P, P]
+        lib.oracle_gather_cache.restype = i32
+        lib.oracle_gather_cache.argtypes = [P, i64, i32, i32, flt, P, i32, P, P, i32, P, i64]
         lib.oracle_num_cores.restype = i32
         lib.oracle_num_cores.argtypes = []
         _lib = lib
@@ -117,6 +119,24 @@ def cache_write(kv_c: np.ndarray, k_pe: np.ndarray, slot_mapping: np.ndarray, ca
                                     cache.shape[0], page_size, cache_dtype, float(kv_scale))
     if rc != 0:
         raise ValueError("oracle_cache_write: slot out of range")
+
+
+# ----------------------------------------------------------- context gather
+
+def gather_cache(cache: np.ndarray, page_size: int, cache_dtype: int, kv_scale: float, block_table: np.ndarray,
+                 cu_seq_lens: np.ndarray, seq_starts, dst_rows: int) -> np.ndarray:
+    """gather_and_maybe_dequant_cache: bf16 bits [dst_rows, 576]; rows past
+    cu_seq_lens[-1] are left zero."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seq_lens, dtype=np.int32)
+    st = None if seq_starts is None else np.ascontiguousarray(seq_starts, dtype=np.int32)
+    dst = np.zeros((dst_rows, DQK), dtype=np.uint16)
+    rc = _load().oracle_gather_cache(_ptr(cache), cache.shape[0], page_size, cache_dtype, float(kv_scale),
+                                     _ptr(bt), bt.shape[1], _ptr(cu), _ptr(st) if st is not None else None,
+                                     cu.size - 1, _ptr(dst), dst_rows)
+    if rc != 0:
+        raise ValueError("oracle_gather_cache: position, page or destination row out of range")
+    return dst
 
 
 # ------------------------------------------------------------------- decode

@@ -34,6 +34,14 @@
  *    done in float32; dequantisation multiplies by kv_scale
  *    (vllm.model_executor.layers.attention.mla_attention, calc_kv_scales:
  *    k_scale = abs-max / range).
+ *  - oracle_gather_cache: gather_and_maybe_dequant_cache of the chunked
+ *    prefill context path (common.py, MLACommonImpl._compute_prefill_context;
+ *    the chunk metadata of MLACommonMetadataBuilder): request b's rows go to
+ *    dst[cu_seq_lens[b] .. cu_seq_lens[b+1]), row j of them is the latent row
+ *    at context position seq_starts[b] + j, fetched through the block table;
+ *    a bf16 cache is copied, an e4m3 cache is dequantised to the model dtype
+ *    as bf16(float32(code) * kv_scale) (float32 product, then round to
+ *    nearest even).
  *  - e4m3: OCP FP8 E4M3 ("fn") -- 1 sign, 4 exponent (bias 7), 3 mantissa
  *    bits, no infinities, S.1111.111 is NaN, largest finite 448; encoding
  *    rounds to nearest, ties to even, and saturates finite overflow to +-448.
@@ -154,6 +162,49 @@ int oracle_cache_write(const uint16_t *kv_c, const uint16_t *k_pe, const int64_t
                 float v = (float)oracle_bf16_to_f64(x);
                 float scaled = v / kv_scale;      /* float32, correctly rounded */
                 ((uint8_t *)cache)[slot * ORC_DQK + d] = oracle_f32_to_e4m3(scaled);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------- context gather */
+
+/* float32 -> bf16 bits, round to nearest, ties to even (NaN stays a quiet NaN). */
+static uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1;
+    return (uint16_t)keep;
+}
+
+int oracle_gather_cache(const void *cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
+                        const int32_t *block_table, int max_pages, const int32_t *cu_seq_lens,
+                        const int32_t *seq_starts, int batch, uint16_t *dst, int64_t dst_rows)
+{
+    for (int b = 0; b < batch; ++b) {
+        int64_t n = (int64_t)cu_seq_lens[b + 1] - cu_seq_lens[b];
+        for (int64_t j = 0; j < n; ++j) {
+            int64_t pos = (int64_t)(seq_starts ? seq_starts[b] : 0) + j;
+            int64_t r = cu_seq_lens[b] + j;
+            if (r < 0 || r >= dst_rows || pos < 0 || pos >= (int64_t)max_pages * page_size)
+                return -1;
+            int64_t page = block_table[(int64_t)b * max_pages + pos / page_size];
+            if (page < 0 || page >= num_blocks)
+                return -1;
+            int64_t row = page * page_size + pos % page_size;
+            for (int d = 0; d < ORC_DQK; ++d) {
+                if (cache_dtype == ORC_CACHE_BF16) {
+                    dst[r * ORC_DQK + d] = ((const uint16_t *)cache)[row * ORC_DQK + d];
+                } else {
+                    float v = (float)oracle_e4m3_to_f64(((const uint8_t *)cache)[row * ORC_DQK + d]);
+                    dst[r * ORC_DQK + d] = oracle_f32_to_bf16(v * kv_scale);   /* float32 product */
+                }
             }
         }
     }

@@ -355,3 +355,78 @@ def test_cache_write_fp8_is_rne_of_x_over_scale():
     assert np.array_equal(got, ref.view(torch.uint8).numpy())
     deq = oracle.e4m3_to_f64(got) * case.kv_scale
     assert np.max(np.abs(deq - x)) <= case.kv_scale * 16      # half ulp at the top binade (32/2)
+
+
+# -------------------------------------------------------------- context gather
+
+def _golden_e4m3():
+    """code -> value from the OCP E4M3 table of tests/golden/e4m3_values.txt."""
+    import os
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "e4m3_values.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        code, val = line.split()[:2]
+        vals[int(code, 0)] = float(val)
+    return vals
+
+
+def test_gather_bf16_is_the_position_ordered_rows():
+    """Gathering whole contexts from position 0 returns each request's rows in
+    position order (the test-side gather), bit for bit; a chunk that starts
+    mid-page returns the same rows shifted."""
+    case = synth.make_decode_case(num_heads=2, batch=5, ctx=(30, 300), page_size=16, seed=51, poison=False)
+    lens = case.seq_lens.astype(np.int64)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    got = oracle.gather_cache(case.pool, 16, oracle.CACHE_BF16, 1.0, case.block_table, cu, None, int(cu[-1]) + 3)
+    for b in range(case.batch):
+        assert np.array_equal(got[cu[b]:cu[b + 1]], _rows_in_order(case, b))
+    assert not got[cu[-1]:].any()
+    starts = np.array([7, 0, 21, 3, 16], dtype=np.int32)
+    n = np.minimum(lens - starts, 40)
+    cu2 = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    got2 = oracle.gather_cache(case.pool, 16, oracle.CACHE_BF16, 1.0, case.block_table, cu2, starts, int(cu2[-1]))
+    for b in range(case.batch):
+        assert np.array_equal(got2[cu2[b]:cu2[b + 1]], _rows_in_order(case, b)[starts[b]:starts[b] + n[b]])
+
+
+def test_gather_e4m3_dequantises_to_table_values():
+    """With a power-of-two scale the dequantised value code * scale is exact in
+    bf16: every gathered element equals the OCP table value times the scale
+    (NaN codes stay NaN).  Codes are drawn from the golden table's entries."""
+    table = _golden_e4m3()
+    nb, ps = 4, 16
+    rng = np.random.Generator(np.random.PCG64(52))
+    codes = np.array(sorted(table) + [0x7F, 0xFF], dtype=np.uint8)     # table values and the two NaNs
+    cache = rng.choice(codes, size=(nb, ps, DQK))
+    bt = np.array([[2, 0], [3, 1]], dtype=np.int32)
+    cu = np.array([0, 20, 45], dtype=np.int32)
+    got = oracle.gather_cache(cache, ps, oracle.CACHE_E4M3, 0.125, bt, cu, np.array([5, 0], np.int32), 45)
+    vals = oracle.bf16_to_f64(got)
+    for b, (lo, hi) in enumerate([(0, 20), (20, 45)]):
+        start = 5 if b == 0 else 0
+        for j in range(hi - lo):
+            pos = start + j
+            codes = cache[bt[b, pos // ps], pos % ps]
+            want = np.array([table[c] * 0.125 if c in table else np.nan for c in codes])
+            row = vals[lo + j]
+            assert np.array_equal(np.isnan(row), np.isnan(want))
+            assert np.array_equal(row[~np.isnan(want)], want[~np.isnan(want)])
+
+
+def test_gather_e4m3_rounding_matches_torch():
+    """With an arbitrary scale the float32 product is rounded to bf16: the
+    oracle agrees bit for bit with torch's float8 -> float32 multiply ->
+    bfloat16 cast on every finite code."""
+    nb, ps = 2, 32
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    rng = np.random.Generator(np.random.PCG64(53))
+    cache = rng.choice(finite, size=(nb, ps, DQK))
+    scale = np.float32(0.0137)
+    bt = np.array([[1, 0]], dtype=np.int32)
+    got = oracle.gather_cache(cache, ps, oracle.CACHE_E4M3, float(scale), bt, np.array([0, 64], np.int32), None, 64)
+    rows = np.concatenate([cache[1], cache[0]])
+    t = torch.from_numpy(rows).view(torch.float8_e4m3fn).float() * torch.tensor(scale)
+    want = t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
