@@ -7,10 +7,12 @@ Default workload: DeepSeek-V3-shaped decode, N=128 heads, batch 64, contexts
 uniform in [1024, 8192], page 64, bf16 cache in a 40k-page pool.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                       [--workload NAME] [--op decode|q_absorb|v_up_proj]
+                       [--workload NAME] [--op decode|q_absorb|v_up_proj|gather]
 --op q_absorb / v_up_proj times the per-head projections around the decode
 (query absorption q_nope @ W_UK_T, value up-projection o_latent @ W_UV) on
-the workload's token and head counts instead of the decode step.
+the workload's token and head counts instead of the decode step; --op gather
+times the paged context gather (gather_and_maybe_dequant_cache) of every
+request's whole context.
 Prints one JSON line.  With --gpus N > 1 (under torchrun) every rank runs an
 independent replica (the decode of one batch does not shard), value = tokens of
 all ranks / max time over ranks.  --impl reference times the fp64 CPU oracle
@@ -531,6 +533,109 @@ def run_proj(args):
     return res
 
 
+def run_gather(args):
+    """--op gather: gather_and_maybe_dequant_cache of every request's whole
+    context (cu_seq_lens = cumsum(seq_lens), chunk starts 0) into a dense bf16
+    workspace, K launches back to back (the cache rows read and the rows
+    written, ~2 x 340 MB, are far larger than L2)."""
+    import torch
+    import mla_latent_kv_15_gb300 as mla
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    mla.load()
+    case = synth.workload(args.workload, poison=False)
+    dev = "cuda"
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    if case.cache_dtype == "bf16":
+        cache = bf16(case.pool)
+    else:                                  # quantised on the GPU by the library's cache write
+        cache = torch.zeros(case.pool.shape, dtype=torch.uint8, device=dev).view(torch.float8_e4m3fn)
+        flat = case.pool.reshape(-1, synth.DQK)[case.referenced_slots]
+        mla.cache_write(bf16(flat[:, :synth.LKV]), bf16(flat[:, synth.LKV:]),
+                        torch.from_numpy(case.referenced_slots).to(dev), cache, case.kv_scale)
+    lens = case.seq_lens.astype(np.int64)
+    cu_h = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+    rows = int(cu_h[-1])
+    bt_h = torch.from_numpy(case.block_table)
+    cu, bt = cu_h.to(dev), bt_h.to(dev)
+    dst = torch.empty((rows, synth.DQK), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def op(c=cu, b=bt):
+        mla.gather_cache(cache, b, c, dst, kv_scale=case.kv_scale, status=status)
+
+    for _ in range(args.warmup):
+        op()
+    torch.cuda.synchronize()
+    t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    with sampler:
+        host_lead(stream)
+        t_a.record(stream)
+        for _ in range(args.steps):
+            op()
+        t_b.record(stream)
+        torch.cuda.synchronize()
+    ms = t_a.elapsed_time(t_b) / args.steps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"gather reported device error word {int(status.item())}")
+    # e2e: block table and cu_seq_lens in from pinned host memory, the gathered rows back
+    cu_p, bt_p = cu_h.pin_memory(), bt_h.pin_memory()
+    dst_h = torch.empty(dst.shape, dtype=dst.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e_steps):
+        cu.copy_(cu_p, non_blocking=True)
+        bt.copy_(bt_p, non_blocking=True)
+        op()
+        dst_h.copy_(dst, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    row_bytes = synth.DQK * (2 if case.cache_dtype == "bf16" else 1)
+    alg = rows * (row_bytes + synth.DQK * 2) + cu_h.numel() * 4 + bt_h.numel() * 4
+    hbm, _, src = peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    res = {
+        "metric": f"context gather rows/s + HBM GB/s & % roofline ({case.cache_dtype} cache -> bf16 rows)",
+        "op": "gather", "value": round(rows / (ms * 1e-3), 1), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if case.cache_dtype == "bf16" else "e4m3->bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: every request's whole context", "rows": rows,
+                   "batch": case.batch, "page_size": case.page_size,
+                   "l2": "no flush: each launch reads and writes ~2 x 340 MB, far more than L2",
+                   "timing": f"one CUDA event pair around {args.steps} back-to-back launches"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": profiled_traffic(args.workload, [f"gather_{args.workload}.md"], "gather.cu"),
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)", "algorithmic_bytes_per_launch": alg},
+        "e2e": {"value": round(rows / (e2e_ms * 1e-3), 1), "unit": "rows/s",
+                "h2d_bytes_per_step": cu_p.numel() * 4 + bt_p.numel() * 4,
+                "d2h_bytes_per_step": dst_h.numel() * 2,
+                "copies": "pinned host buffers, copies and launch serialised on one stream"},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        host_cache = case.pool if case.cache_dtype == "bf16" else oracle.prepare_cache(case, with_new_rows=False)
+        nb = min(case.batch, 16)
+        t0 = time.perf_counter()
+        oracle.gather_cache(host_cache, case.page_size,
+                            oracle.CACHE_BF16 if case.cache_dtype == "bf16" else oracle.CACHE_E4M3, case.kv_scale,
+                            case.block_table[:nb], cu_h.numpy()[:nb + 1], None, int(cu_h[nb]))
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": round(int(cu_h[nb]) / el, 3), "unit": "rows/s", "cores": 1,
+                               "kind": "oracle", "sample": f"{nb} of {case.batch} requests' contexts, {el:.2f} s"}
+    return res
+
+
 def run_proj_reference(args):
     """--impl reference --op ...: the oracle's fp64 einsum for the projection,
     timed on the host over K steps of the same inputs as the GPU arm."""
@@ -584,11 +689,17 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="decode", choices=["decode", "q_absorb", "v_up_proj"])
+    ap.add_argument("--op", default="decode", choices=["decode", "q_absorb", "v_up_proj", "gather"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    if args.op != "decode":
+    if args.op == "gather":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "op": "gather",
+                              "unavailable": "the gather's reference arm is its cpu_baseline leg"}), flush=True)
+            return
+        res = run_gather(args)
+    elif args.op != "decode":
         res = run_proj_reference(args) if args.impl == "reference" else run_proj(args)
     else:
         res = run_reference(args) if args.impl == "reference" else run_gpu(args)

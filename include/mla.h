@@ -275,6 +275,43 @@ MLA_API int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_token
  */
 MLA_API int mla_proj_status(int* status, int clear, void* stream);
 
+/*
+ * mla_gather_cache -- gather_and_maybe_dequant_cache of the chunked-prefill
+ * context path (common.py, MLACommonImpl._compute_prefill_context, with the
+ * chunk metadata of MLACommonMetadataBuilder): copy the latent rows of a
+ * context chunk of every request out of the paged cache into a dense bf16
+ * workspace.
+ *
+ *   dst[cu_seq_lens[b] + j] = row at context position seq_starts[b] + j of
+ *                             request b, j < cu_seq_lens[b+1] - cu_seq_lens[b],
+ *   row at position p = cache[block_table[b, p / page_size], p % page_size]
+ *
+ * A bf16 cache is copied bit for bit; an e4m3 cache is dequantised to
+ * bf16(float32(code) * kv_scale) (float32 product, round to nearest even).
+ *   cache         [num_blocks, page_size, 576] of cache_dtype, 16-byte aligned;
+ *                 page_size >= 1 (chunk starts need not be page aligned)
+ *   block_table   [batch, max_pages_per_seq] int32
+ *   cu_seq_lens   [batch + 1] int32 on the device, cu_seq_lens[0] = 0,
+ *                 non-decreasing
+ *   seq_starts    [batch] int32 on the device, or NULL (every chunk starts at
+ *                 position 0)
+ *   dst           [num_tokens, 576] bf16, 16-byte aligned; num_tokens is its
+ *                 capacity in rows (>= cu_seq_lens[batch]); rows past
+ *                 cu_seq_lens[batch] are not written
+ *   status        one int32 on the device, or NULL: OR of mla_device_error
+ *                 bits -- MLA_DEVERR_BAD_SEQ_LEN: a position outside the
+ *                 block table; MLA_DEVERR_BAD_BLOCK: a page id outside
+ *                 [0, num_blocks); MLA_DEVERR_BAD_QSL: cu_seq_lens[batch] >
+ *                 num_tokens (rows past num_tokens are dropped).  Rows whose
+ *                 position or page is bad are written as zeros.  The word is
+ *                 OR-ed into, never cleared.
+ * num_tokens == 0 or batch == 0 is a no-op.  One launch.
+ */
+MLA_API int mla_gather_cache(const void* cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
+                             const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seq_lens,
+                             const int32_t* seq_starts, int batch, void* dst, int64_t num_tokens, int32_t* status,
+                             void* stream);
+
 /* Human-readable description of the calling thread's last error ("" if none). */
 MLA_API const char* mla_last_error(void);
 

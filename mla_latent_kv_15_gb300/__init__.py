@@ -28,7 +28,8 @@ DQK = 576
 
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
-                 "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status")
+                 "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
+                 "mla_gather_cache")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -71,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_q_absorb.argtypes = [P, i64, P, i64, i32, i32, P, P]
     lib.mla_v_up_proj.restype = i32
     lib.mla_v_up_proj.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.mla_gather_cache.restype = i32
+    lib.mla_gather_cache.argtypes = [P, i64, i32, i32, f32, P, i32, P, P, i32, P, i64, P, P]
     lib.mla_proj_status.restype = i32
     lib.mla_proj_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
     _lib = lib
@@ -172,6 +175,18 @@ def v_up_proj(o_lat, w_uv, out, stream=None) -> None:
     """out[t, n, :] = o_lat[t, n, :] @ w_uv[n] (bf16; w_uv [N, 512, V], out [T, N, V])."""
     T, N, _ = o_lat.shape
     _check(load().mla_v_up_proj(_ptr(o_lat), _ptr(w_uv), T, N, w_uv.shape[2], _ptr(out), _stream(stream)))
+
+
+def gather_cache(cache, block_table, cu_seq_lens, dst, seq_starts=None, kv_scale: float = 1.0, status=None,
+                 stream=None) -> None:
+    """gather_and_maybe_dequant_cache: dst [num_tokens, 576] bf16 receives the
+    chunk rows of every request (cu_seq_lens [B+1], seq_starts [B] int32)."""
+    nb, ps, w = cache.shape
+    assert w == DQK
+    B = cu_seq_lens.numel() - 1
+    _check(load().mla_gather_cache(_ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale), _ptr(block_table),
+                                   block_table.shape[1], _ptr(cu_seq_lens), _ptr(seq_starts), B, _ptr(dst),
+                                   dst.shape[0], _ptr(status), _stream(stream)))
 
 
 def proj_status(clear: bool = False, stream=None) -> int:

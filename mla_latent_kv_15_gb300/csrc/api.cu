@@ -276,6 +276,30 @@ int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_tokens, int n
                    stream);
 }
 
+int mla_gather_cache(const void* cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
+                     const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seq_lens,
+                     const int32_t* seq_starts, int batch, void* dst, int64_t num_tokens, int32_t* status,
+                     void* stream) {
+  if (num_tokens < 0 || batch < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens and batch must be >= 0");
+  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
+  if (num_tokens == 0 || batch == 0) return ok();
+  if (page_size < 1 || num_blocks < 1 || max_pages_per_seq < 1)
+    return fail(MLA_ERR_INVALID_ARG, "page_size, num_blocks and max_pages_per_seq must be positive");
+  if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
+  if (!cache || !block_table || !cu_seq_lens || !dst) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(cache, 16) || !aligned(dst, 16)) return fail(MLA_ERR_INVALID_ARG, "cache and dst must be 16-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(cu_seq_lens, 4) || (seq_starts && !aligned(seq_starts, 4)) ||
+      (status && !aligned(status, 4)))
+    return fail(MLA_ERR_INVALID_ARG, "block_table, cu_seq_lens, seq_starts and status must be 4-byte aligned");
+  cudaError_t e = mla::launch_gather(cache, num_blocks, page_size, cache_dtype == MLA_FP8_E4M3, kv_scale,
+                                     block_table, max_pages_per_seq, cu_seq_lens, seq_starts, batch, dst,
+                                     num_tokens, status, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return ok();
+}
+
 int mla_proj_status(int* status, int clear, void* stream) {
   if (!status) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
   cudaError_t e = mla::head_proj_status(status, clear, (cudaStream_t)stream);

@@ -106,6 +106,23 @@ def test_projection_validation_rejects_before_launch(lib):
     assert lib.mla_proj_status(None, 0, None) == -1
 
 
+def test_gather_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    c, bt, cu, d = P(1 << 20), P(1 << 24), P(1 << 26), P(1 << 28)    # never dereferenced
+    assert lib.mla_gather_cache(c, 10, 64, 3, 1.0, bt, 4, cu, None, 2, d, 100, None, None) == -1
+    assert b"cache_dtype" in lib.mla_last_error()
+    assert lib.mla_gather_cache(c, 10, 0, 0, 1.0, bt, 4, cu, None, 2, d, 100, None, None) == -1
+    assert lib.mla_gather_cache(c, 10, 64, 1, 0.0, bt, 4, cu, None, 2, d, 100, None, None) == -1
+    assert b"kv_scale" in lib.mla_last_error()
+    assert lib.mla_gather_cache(c, 10, 64, 0, 1.0, bt, 4, None, None, 2, d, 100, None, None) == -1
+    assert lib.mla_gather_cache(P((1 << 20) + 8), 10, 64, 0, 1.0, bt, 4, cu, None, 2, d, 100, None, None) == -1
+    assert lib.mla_gather_cache(c, 10, 64, 0, 1.0, bt, 4, cu, None, 2, d, 100, P((1 << 20) + 2), None) == -1
+    assert lib.mla_gather_cache(c, 10, 64, 0, 1.0, bt, 4, cu, None, 2, d, -1, None, None) == -1
+    # nothing to gather: no-op
+    assert lib.mla_gather_cache(None, 0, 0, 0, 0.0, None, 0, None, None, 0, None, 0, None, None) == 0
+    assert lib.mla_last_error() == b""
+
+
 def test_product_fails_loudly_without_library(tmp_path):
     """No fallback: a missing library is an ImportError, not a CPU path."""
     import mla_latent_kv_15_gb300 as mla
