@@ -8,8 +8,10 @@
 //
 // An HBM-bound copy: each CTA resolves 16 destination rows (request by
 // binary search over cu_seq_lens, page through the block table), then its
-// 256 threads move the rows with 16-byte loads and stores, so consecutive
-// threads touch consecutive bytes of a row.  Grid-stride over row groups.
+// 256 threads move the rows with 16-byte loads (and 16-byte stores for a bf16
+// cache, 32-byte stores of 16 dequantised values for an e4m3 one), so
+// consecutive threads touch consecutive bytes of a row.  Grid-stride over
+// row groups.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -21,6 +23,7 @@ namespace {
 constexpr int kGRows = 16;       // destination rows per CTA iteration
 constexpr int kGThreads = 256;
 constexpr int kChunks = kDqk * 2 / 16;   // 16-byte pieces of a bf16 row: 72
+constexpr int kChunks8 = kDqk / 16;      // 16-byte pieces of an e4m3 row: 36 (32 output bytes each)
 
 // Two e4m3 codes -> two floats (exact: every e4m3 value is an f16 value).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
@@ -33,6 +36,19 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four e4m3 codes (one 32-bit word, lowest byte first) -> four bf16 values
+// bf16(float32(code) * scale), packed in two words.
+__device__ __forceinline__ uint2 dequant4(uint32_t w, float scale) {
+  const float2 a = e4m3x2_to_float2((uint16_t)(w & 0xFFFF)), b = e4m3x2_to_float2((uint16_t)(w >> 16));
+  return make_uint2(bf16x2_bits(a.x * scale, a.y * scale), bf16x2_bits(b.x * scale, b.y * scale));
+}
+
+__device__ __forceinline__ void st_global_v8(void* p, uint2 a, uint2 b, uint2 c, uint2 d) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(b.x),
+               "r"(b.y), "r"(c.x), "r"(c.y), "r"(d.x), "r"(d.y)
+               : "memory");
 }
 
 template <bool kFp8>
@@ -78,25 +94,36 @@ __global__ void __launch_bounds__(kGThreads) gather_kernel(const uint8_t* __rest
       s_src[threadIdx.x] = src;
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < kGRows * kChunks; c += kGThreads) {
-      const int i = c / kChunks, k = c - i * kChunks;
-      const int64_t src = s_src[i];
-      if (src == -2) continue;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (src >= 0) {
-        if (kFp8) {
-          const uint2 codes = __ldg(reinterpret_cast<const uint2*>(cache + src * kDqk) + k);
-          const float2 a = e4m3x2_to_float2((uint16_t)(codes.x & 0xFFFF)),
-                       b = e4m3x2_to_float2((uint16_t)(codes.x >> 16)),
-                       c2 = e4m3x2_to_float2((uint16_t)(codes.y & 0xFFFF)),
-                       d = e4m3x2_to_float2((uint16_t)(codes.y >> 16));
-          v = make_uint4(bf16x2_bits(a.x * kv_scale, a.y * kv_scale), bf16x2_bits(b.x * kv_scale, b.y * kv_scale),
-                         bf16x2_bits(c2.x * kv_scale, c2.y * kv_scale), bf16x2_bits(d.x * kv_scale, d.y * kv_scale));
+    if (kFp8) {
+      // 16 codes in (one 16-byte load), 32 bytes out (one 32-byte store when
+      // dst is 32-byte aligned, else two 16-byte stores)
+      const bool a32 = (reinterpret_cast<uintptr_t>(dst) & 31) == 0;
+      for (int c = threadIdx.x; c < kGRows * kChunks8; c += kGThreads) {
+        const int i = c / kChunks8, k = c - i * kChunks8;
+        const int64_t src = s_src[i];
+        if (src == -2) continue;
+        uint4 codes = make_uint4(0, 0, 0, 0);
+        if (src >= 0) codes = __ldg(reinterpret_cast<const uint4*>(cache + src * kDqk) + k);
+        const float sc = src >= 0 ? kv_scale : 0.f;
+        uint8_t* out = dst + (r0 + i) * (kDqk * 2) + k * 32;
+        const uint2 v0 = dequant4(codes.x, sc), v1 = dequant4(codes.y, sc), v2 = dequant4(codes.z, sc),
+                    v3 = dequant4(codes.w, sc);
+        if (a32) {
+          st_global_v8(out, v0, v1, v2, v3);
         } else {
-          v = __ldg(reinterpret_cast<const uint4*>(cache + src * (kDqk * 2)) + k);
+          reinterpret_cast<uint4*>(out)[0] = make_uint4(v0.x, v0.y, v1.x, v1.y);
+          reinterpret_cast<uint4*>(out)[1] = make_uint4(v2.x, v2.y, v3.x, v3.y);
         }
       }
-      reinterpret_cast<uint4*>(dst + (r0 + i) * (kDqk * 2))[k] = v;
+    } else {
+      for (int c = threadIdx.x; c < kGRows * kChunks; c += kGThreads) {
+        const int i = c / kChunks, k = c - i * kChunks;
+        const int64_t src = s_src[i];
+        if (src == -2) continue;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (src >= 0) v = __ldg(reinterpret_cast<const uint4*>(cache + src * (kDqk * 2)) + k);
+        reinterpret_cast<uint4*>(dst + (r0 + i) * (kDqk * 2))[k] = v;
+      }
     }
     __syncthreads();
   }

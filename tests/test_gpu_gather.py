@@ -52,6 +52,26 @@ def test_gather_bitexact(dtype, page_size):
     assert np.all(got[cu[-1]:] == np.uint16(0xC0E0))          # bf16 -7.0: rows past the chunk untouched
 
 
+def test_gather_fp8_into_16_byte_aligned_dst():
+    """A destination that is 16- but not 32-byte aligned (the e4m3 path then
+    stores 16 bytes at a time)."""
+    case = synth.make_decode_case(num_heads=2, batch=4, ctx=(40, 300), page_size=64, cache_dtype="fp8", seed=75,
+                                  poison=False)
+    g = GpuCase(case)
+    starts, cu = chunks(case, 76, 200)
+    total = int(cu[-1])
+    buf = torch.zeros((total + 1) * 576 + 8, dtype=torch.bfloat16, device="cuda")
+    dst = buf[8:8 + total * 576].view(total, 576)               # 16 bytes past a 256-byte boundary
+    assert dst.data_ptr() % 32 == 16
+    mla.gather_cache(g.cache, g.block_table, torch.from_numpy(cu).cuda(), dst,
+                     seq_starts=torch.from_numpy(starts).cuda(), kv_scale=case.kv_scale)
+    torch.cuda.synchronize()
+    got = dst.view(torch.int16).cpu().numpy().view(np.uint16)
+    want = oracle.gather_cache(oracle.prepare_cache(case), 64, oracle.CACHE_E4M3, case.kv_scale, case.block_table,
+                               cu, starts, total)
+    assert np.array_equal(got, want)
+
+
 def test_gather_whole_contexts_from_zero():
     """seq_starts = NULL: every request's context from position 0."""
     case = synth.make_decode_case(num_heads=2, batch=5, ctx=(1, 700), page_size=64, seed=73, poison=False)
