@@ -22,8 +22,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const Plan& P = a.plan;
   const int g = blockIdx.x;
-  if (g >= P.header->num_groups) return;
+  // both loads at once (the grid covers the workspace's max_groups records)
+  const int num_groups = P.header->num_groups;
   const GroupRec gr = P.groups[g];
+  if (g >= num_groups) return;
   if (gr.pieces == 1) return;  // written directly by the decode kernel
   const int r = blockIdx.y * 4 + (threadIdx.x >> 6);
   if (r >= gr.nrows) return;
@@ -34,7 +36,42 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
   const int d0 = sub * 8;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   float lse = -INFINITY;
-  if (gr.pieces > 1) {
+  constexpr int kFew = 4;
+  if (gr.pieces <= kFew) {
+    // the usual case: every load of every piece issued before any use
+    float l[kFew];
+    float4 x0[kFew], x1[kFew];
+#pragma unroll
+    for (int i = 0; i < kFew; ++i) {
+      l[i] = -INFINITY;
+      if (i < gr.pieces) {
+        const size_t slot = (size_t)(gr.ubase + i);
+        l[i] = P.part_lse[slot * kRows + r];
+        const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
+        x0[i] = src[0];
+        x1[i] = src[1];
+      }
+    }
+    float mx = l[0];
+#pragma unroll
+    for (int i = 1; i < kFew; ++i) mx = fmaxf(mx, l[i]);
+    if (mx != -INFINITY) {
+      float wsum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kFew; ++i) {
+        if (i < gr.pieces) {
+          const float w = __expf(l[i] - mx);
+          wsum += w;
+          acc[0] += w * x0[i].x; acc[1] += w * x0[i].y; acc[2] += w * x0[i].z; acc[3] += w * x0[i].w;
+          acc[4] += w * x1[i].x; acc[5] += w * x1[i].y; acc[6] += w * x1[i].z; acc[7] += w * x1[i].w;
+        }
+      }
+      const float inv = 1.f / wsum;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] *= inv;
+      lse = mx + __logf(wsum);
+    }
+  } else {
     float mx = -INFINITY;
     for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
     if (mx != -INFINITY) {

@@ -33,6 +33,9 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 // Exclusive scan over the block (blockDim.x == 1024); *total gets the sum.
+constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
+constexpr int kPlanSmemUnits = 2048;    // and units
+
 __device__ int block_excl_scan(int v, int* total) {
   __shared__ int warp_sums[32];
   __shared__ int s_total;
@@ -53,11 +56,19 @@ __device__ int block_excl_scan(int v, int* total) {
   return r;
 }
 
+// kStaged: the group records and unit clusters live in shared memory while
+// the plan is built (each phase reads what other threads wrote in the
+// previous one) and are copied out at the end; for plans that fit.
+template <bool kStaged>
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ qsl, int batch, int N,
                                                     int max_pages, int page_size, int num_splits, int C,
                                                     int GR, Plan P) {
   __shared__ int s_flags;
+  __shared__ GroupRec s_groups[kStaged ? kPlanSmemGroups : 1];
+  __shared__ int s_ucl[kStaged ? kPlanSmemUnits : 1];
+  GroupRec* grp = kStaged ? s_groups : P.groups;
+  int* ucl = kStaged ? s_ucl : P.unit_cluster;
   const int tid = threadIdx.x;
   // Launched as a programmatic dependent of the kernel before it on the
   // stream, so only its launch overlaps that kernel's tail: it waits for that
@@ -103,7 +114,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         r.pieces = 0;
         r.ubase = 0;
         r.tpos = 0;
-        P.groups[gb + g] = r;
+        grp[gb + g] = r;
       }
     }
     carry += total;
@@ -119,10 +130,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   carry = 0;
   for (int base = 0; base < G; base += 1024) {
     const int g = base + tid;
-    const int t = g < G ? P.groups[g].tiles : 0;
+    const int t = g < G ? grp[g].tiles : 0;
     int total;
     const int pos = block_excl_scan(t, &total) + carry;
-    if (g < G) P.groups[g].tpos = pos;
+    if (g < G) grp[g].tpos = pos;
     carry += total;
   }
   const int T = carry;
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const int g = base + tid;
     int pieces = 0;
     if (g < G) {
-      const GroupRec r = P.groups[g];
+      const GroupRec r = grp[g];
       if (r.tiles > 0) {
         if (num_splits > 0)
           pieces = min(num_splits, r.tiles);
@@ -146,15 +157,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     int total;
     const int ub = block_excl_scan(pieces, &total) + carry;
     if (g < G) {
-      P.groups[g].pieces = pieces;
-      P.groups[g].ubase = ub;
+      grp[g].pieces = pieces;
+      grp[g].ubase = ub;
     }
     carry += total;
   }
   int U = carry;
   if (U > P.max_units) {  // cannot happen for a workspace sized for num_splits
     __syncthreads();
-    for (int g = tid; g < G; g += 1024) P.groups[g].pieces = 0;
+    for (int g = tid; g < G; g += 1024) grp[g].pieces = 0;
     if (tid == 0) atomicOr(&s_flags, 8);
     U = 0;
   }
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
   // 4. units
   for (int g = tid; g < G; g += 1024) {
-    const GroupRec r = P.groups[g];
+    const GroupRec r = grp[g];
     for (int i = 0; i < r.pieces; ++i) {
       UnitRec u;
       int cl;
@@ -178,19 +189,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       }
       u.slot = r.pieces > 1 ? r.ubase + i : -1;
       P.units[r.ubase + i] = u;
-      P.unit_cluster[r.ubase + i] = cl;
+      ucl[r.ubase + i] = cl;
     }
   }
   __syncthreads();
 
   // 5. first unit of every cluster (unit clusters are non-decreasing)
   for (int u = tid; u < U; u += 1024) {
-    const int c = P.unit_cluster[u];
-    const int cp = u > 0 ? P.unit_cluster[u - 1] : -1;
+    const int c = ucl[u];
+    const int cp = u > 0 ? ucl[u - 1] : -1;
     for (int k = cp + 1; k <= c; ++k) P.cluster_begin[k] = u;
+    if (kStaged) P.unit_cluster[u] = c;
   }
+  if (kStaged)
+    for (int g = tid; g < G; g += 1024) P.groups[g] = grp[g];
   if (tid == 0) {
-    const int last = U > 0 ? P.unit_cluster[U - 1] : -1;
+    const int last = U > 0 ? ucl[U - 1] : -1;
     for (int k = last + 1; k <= kMaxClusters; ++k) P.cluster_begin[k] = U;
     PlanHeader h;
     h.status = s_flags;
@@ -217,8 +231,9 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, qsl, batch, num_heads, max_pages, page_size,
-                                     num_splits, num_clusters, group_rows, plan);
+  const bool staged = plan.max_groups <= kPlanSmemGroups && plan.max_units <= kPlanSmemUnits;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, staged ? plan_kernel<true> : plan_kernel<false>, seq_lens, qsl, batch,
+                                     num_heads, max_pages, page_size, num_splits, num_clusters, group_rows, plan);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
