@@ -72,6 +72,22 @@ def profiled_traffic(workload: str, names=None, source: str = "decode.cu"):
     return None
 
 
+def max_over_ranks(values, dist, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    job's time); identity on one process."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job rate: the units all ranks processed / the max-over-ranks time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def host_lead(stream, ms: float = 5.0):
     """Keep the GPU busy (a spin kernel of ~`ms` at the maximum clock) while the
     host enqueues the timed launches that follow, so that no timed interval
@@ -298,10 +314,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = e2e_start.elapsed_time(e2e_end) / args.steps
 
-    if dist:
-        t = torch.tensor([ms, kms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kms, e2e_ms = t.tolist()
+    ms, kms, e2e_ms = max_over_ranks([ms, kms, e2e_ms], dist, dev)
     if rank != 0:
         return None
 
@@ -321,7 +334,7 @@ def run_gpu(args):
     roof.update({"traffic": traffic,
                  "peak_source": f"{src} (MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'})",
                  "algorithmic_bytes_per_launch": alg["decode_bytes"], "algorithmic_flops_per_launch": alg["flops"]})
-    tok_s = world * T / (ms * 1e-3)
+    tok_s = job_throughput(T, world, ms)
     clocks = sampler.summary()
     res = {
         "metric": METRIC,
@@ -348,7 +361,7 @@ def run_gpu(args):
         "tflops": round(achieved_tf, 1),
         "decode_kernel_ms": round(kms, 5),
         "roofline": roof,
-        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(job_throughput(T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": inp_bytes, "d2h_bytes_per_step": out_bytes,
                 "copies": "pinned host buffers; step i+1's inputs and step i's outputs move on copy streams "
                           "while step i computes (two device buffer sets)"},
