@@ -38,7 +38,7 @@ def check(got: torch.Tensor, ref: np.ndarray):
 
 
 @pytest.mark.parametrize("T,N,V", [(1, 1, 128), (5, 16, 128), (64, 128, 128), (130, 3, 64), (257, 2, 192),
-                                   (33, 4, 256), (7, 2, 512)])
+                                   (33, 4, 256), (7, 2, 512), (70, 2, 1024), (600, 4, 128)])
 def test_v_up_proj(T, N, V):
     """out[t, n, :] = o_lat[t, n, :] @ W_UV[n]: token tiles with ragged tails,
     every supported width (one and several column tiles)."""
@@ -54,7 +54,8 @@ def test_v_up_proj(T, N, V):
 
 
 @pytest.mark.parametrize("T,N,P,stride", [(1, 1, 128, 128), (64, 128, 128, 192), (130, 16, 128, 192),
-                                          (9, 3, 64, 64), (200, 2, 256, 320)])
+                                          (9, 3, 64, 64), (200, 2, 256, 320), (3, 2, 1024, 1024),
+                                          (300, 8, 512, 576)])
 def test_q_absorb(T, N, P, stride):
     """ql_nope[t, n, :] = q_nope[t, n, :] @ W_UK_T[n], q_nope read as the first
     P columns of wider rows (q = [q_nope | q_pe]) when stride > P."""
@@ -67,6 +68,18 @@ def test_q_absorb(T, N, P, stride):
     mla.q_absorb(q_dev[:, :, :P], w_dev, ql)
     torch.cuda.synchronize()
     check(ql, ref)
+    assert mla.proj_status() == 0
+
+
+def test_projection_empty_batch_is_a_no_op():
+    w = torch.zeros((2, 512, 128), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((0, 2, 512), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    mla.v_up_proj(x, w, y)
+    mla.q_absorb(torch.zeros((0, 2, 128), dtype=torch.bfloat16, device="cuda"),
+                 torch.zeros((2, 128, 512), dtype=torch.bfloat16, device="cuda"),
+                 torch.zeros((0, 2, 512), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
     assert mla.proj_status() == 0
 
 
