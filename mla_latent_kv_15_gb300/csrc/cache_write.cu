@@ -29,6 +29,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const __nv_bfloat16* _
                                                           const int64_t* __restrict__ slots, int64_t num_tokens,
                                                           void* __restrict__ cache, int64_t num_slots,
                                                           float kv_scale) {
+  // Launched as a programmatic dependent: only the launch overlaps the
+  // previous kernel (which may still read the cache or have written the
+  // inputs); every CTA waits for it before touching memory, so the grid also
+  // completes after it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t tok = blockIdx.x * 8LL + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= num_tokens) return;
@@ -66,10 +71,20 @@ cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t
   const int64_t blocks = (num_tokens + 7) / 8;
   const auto* c = static_cast<const __nv_bfloat16*>(kv_c);
   const auto* p = static_cast<const __nv_bfloat16*>(k_pe);
-  if (cache_fp8)
-    cache_write_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(c, p, slots, num_tokens, cache, num_slots, kv_scale);
-  else
-    cache_write_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(c, p, slots, num_tokens, cache, num_slots, kv_scale);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cache_fp8 ? cudaLaunchKernelEx(&cfg, cache_write_kernel<true>, c, p, slots, num_tokens, cache,
+                                                 num_slots, kv_scale)
+                            : cudaLaunchKernelEx(&cfg, cache_write_kernel<false>, c, p, slots, num_tokens, cache,
+                                                 num_slots, kv_scale);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
