@@ -558,13 +558,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       const int q0 = a.qsl ? a.qsl[b] : b;
       const int R = gr.row0 + row;
       const bool valid = row < gr.nrows && R < a.total_rows;
-      int Lr = 0;
+      // Padding rows (past the group) are never stored: they are not masked
+      // and never rescale O, so they cost a warp no work beyond the valid rows'.
+      int Lr = 0x7fffffff;
       if (valid) {
         const int tloc = R / a.num_heads - q0;
         Lr = a.seq_lens[b] - sq + 1 + tloc;
         Lr = Lr < 0 ? 0 : (Lr > gr.lmax ? gr.lmax : Lr);
       }
-      // the warp needs masking only on tiles that reach past its shortest row
+      // the warp needs masking only on tiles that reach past its shortest valid row
       const int lmin_warp = __reduce_min_sync(0xffffffffu, Lr);
       const uint32_t nbytes = (uint32_t)gr.nrows * (kTile * 2);
 
@@ -646,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) *
                            a.scale_log2;
         float alpha = 1.f;
-        if (tmax > m + kRescaleThreshold) {
+        if (valid && tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
           l *= alpha;
           m = tmax;
