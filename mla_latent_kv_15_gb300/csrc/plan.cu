@@ -34,6 +34,13 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 
 // Exclusive scan over the block (blockDim.x == 1024); *total gets the sum.
 constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
+// Fixed cost of a work unit in tiles of decode time: loading the group's
+// query into tensor memory, refilling the pipeline and the epilogue (measured
+// with clock64 on the DeepSeek-V3-shaped batch: ~11.5k cycles per unit
+// against ~3350 per 64-key tile).  Each group is placed on the balanced axis
+// behind this many virtual tiles, so that CTA pairs starting more groups get
+// fewer real tiles.
+constexpr int kUnitCostTiles = 3;
 constexpr int kPlanSmemUnits = 2048;    // and units
 
 __device__ int block_excl_scan(int v, int* total) {
@@ -126,11 +133,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
   __syncthreads();
 
-  // 2. flattened tile positions
+  // 2. positions on the balanced axis: every group with keys spans its
+  //    virtual unit-cost tiles, then its real tiles
   carry = 0;
   for (int base = 0; base < G; base += 1024) {
     const int g = base + tid;
-    const int t = g < G ? grp[g].tiles : 0;
+    const int tl = g < G ? grp[g].tiles : 0;
+    const int t = tl > 0 ? tl + kUnitCostTiles : 0;
     int total;
     const int pos = block_excl_scan(t, &total) + carry;
     if (g < G) grp[g].tpos = pos;
@@ -148,10 +157,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (g < G) {
       const GroupRec r = grp[g];
       if (r.tiles > 0) {
+        const int s0 = r.tpos + kUnitCostTiles;   // first real tile on the axis
         if (num_splits > 0)
           pieces = min(num_splits, r.tiles);
         else
-          pieces = (r.tpos + r.tiles - 1) / W - r.tpos / W + 1;
+          pieces = (s0 + r.tiles - 1) / W - s0 / W + 1;
       }
     }
     int total;
@@ -174,6 +184,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   // 4. units
   for (int g = tid; g < G; g += 1024) {
     const GroupRec r = grp[g];
+    const int s0 = r.tpos + kUnitCostTiles;       // first real tile on the axis
     for (int i = 0; i < r.pieces; ++i) {
       UnitRec u;
       int cl;
@@ -181,11 +192,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       if (num_splits > 0) {
         u.tile_begin = (int)((long long)i * r.tiles / r.pieces);
         u.tile_end = (int)((long long)(i + 1) * r.tiles / r.pieces);
-        cl = min(C - 1, (r.tpos + (u.tile_begin + u.tile_end) / 2) / W);
+        cl = min(C - 1, (s0 + (u.tile_begin + u.tile_end) / 2) / W);
       } else {
-        cl = r.tpos / W + i;
-        u.tile_begin = max(r.tpos, cl * W) - r.tpos;
-        u.tile_end = min(r.tpos + r.tiles, (cl + 1) * W) - r.tpos;
+        cl = s0 / W + i;
+        u.tile_begin = max(s0, cl * W) - s0;
+        u.tile_end = min(s0 + r.tiles, (cl + 1) * W) - s0;
       }
       u.slot = r.pieces > 1 ? r.ubase + i : -1;
       P.units[r.ubase + i] = u;
