@@ -696,11 +696,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       tc_fence_after();
       const float inv = l > 0.f ? a.out_scale / l : 0.f;
       const float lse_nat = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t o[32];
-        tmem_ld32(tl + kTmemO + ch * 32, o);
-        tmem_wait_ld();
-        if (!valid) continue;
+      // one row's 32 output dims (columns 32ch.. of O): bf16 output or fp32 partial
+      auto store_chunk = [&](int ch, const uint32_t (&o)[32]) {
         const int d0 = 256 * rank + 32 * ch;
         // whole 32-byte sectors per store where the address allows (a row is
         // one thread's: 16-byte stores would write half sectors)
@@ -731,6 +728,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
                          __float_as_uint(__uint_as_float(o[8 * v + 6]) * inv),
                          __float_as_uint(__uint_as_float(o[8 * v + 7]) * inv));
         }
+      };
+      // two 32-column loads of O per wait: four round trips to TMEM, not eight
+#pragma unroll 1
+      for (int cp = 0; cp < 4; ++cp) {
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tl + kTmemO + cp * 64, oa);
+        tmem_ld32(tl + kTmemO + cp * 64 + 32, ob);
+        tmem_wait_ld();
+        if (!valid) continue;
+        store_chunk(2 * cp, oa);
+        store_chunk(2 * cp + 1, ob);
       }
       if (valid && rank == 0) {
         if (ur.slot < 0) {
