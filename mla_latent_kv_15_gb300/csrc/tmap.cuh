@@ -24,7 +24,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 
 // 2-D row-major tensor [rows, cols] of `elem_bytes`-byte elements with a row
 // pitch of `row_stride_bytes`; boxes of box_rows x box_cols; out-of-bounds
-// elements read as zero.  Returns false if the driver rejects the layout.
+// elements read as zero.  Returns false if the CUDA driver rejects the layout.
 inline bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t cols,
                            uint64_t rows, uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                            CUtensorMapSwizzle swizzle) {
