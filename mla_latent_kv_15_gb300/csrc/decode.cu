@@ -484,7 +484,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
     const int row = q4 * 32 + lane;          // query row of this thread in the unit
     const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
     const int tid128 = threadIdx.x - 32 * R::kSoftmax0;
-    const uint32_t xrow = (uint32_t)row * (kTile * 2);
+    // receive buffers are chunk-major, [8][kXRows][16 B]: the 32 lanes of a
+    // warp write (and read) 512 contiguous bytes per instruction
+    const uint32_t xrow = (uint32_t)row * 16;
+    constexpr uint32_t kXChunk = (uint32_t)kXRows * 16;
     const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
@@ -521,7 +524,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         const uint32_t bar = xfull_peer0 + b * 8;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          st_async_v4(base + ((c ^ (row & 7)) << 4), pack_f16x2(src[8 * c], src[8 * c + 1]),
+          st_async_v4(base + c * kXChunk, pack_f16x2(src[8 * c], src[8 * c + 1]),
                       pack_f16x2(src[8 * c + 2], src[8 * c + 3]), pack_f16x2(src[8 * c + 4], src[8 * c + 5]),
                       pack_f16x2(src[8 * c + 6], src[8 * c + 7]), bar);
       }
@@ -535,7 +538,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       const uint32_t base = xrecv0 + b * kXBytes + xrow;
 #pragma unroll
       for (int c = 0; c < 8 && row < kXRows; ++c) {
-        const uint4 v = lds128(base + ((c ^ (row & 7)) << 4));
+        const uint4 v = lds128(base + c * kXChunk);
         const float2 f0 = unpack_f16x2(v.x), f1 = unpack_f16x2(v.y), f2 = unpack_f16x2(v.z), f3 = unpack_f16x2(v.w);
         add2(acc[8 * c + 0], acc[8 * c + 1], f0.x, f0.y);
         add2(acc[8 * c + 2], acc[8 * c + 3], f1.x, f1.y);
