@@ -652,6 +652,38 @@ def run_gather(args):
     return res
 
 
+def run_gather_reference(args):
+    """--impl reference --op gather: the oracle's C gather (one thread) of the
+    first 16 requests' whole contexts per step."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    import oracle
+    case = synth.workload(args.workload, poison=False)
+    host_cache = case.pool if case.cache_dtype == "bf16" else oracle.prepare_cache(case, with_new_rows=False)
+    nb = min(case.batch, 16)
+    cu = np.concatenate([[0], np.cumsum(case.seq_lens.astype(np.int64))]).astype(np.int32)[:nb + 1]
+    dt = oracle.CACHE_BF16 if case.cache_dtype == "bf16" else oracle.CACHE_E4M3
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gather_cache(host_cache, case.page_size, dt, case.kv_scale, case.block_table[:nb], cu, None,
+                            int(cu[-1]))
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    v = int(cu[-1]) / (ms * 1e-3)
+    return {
+        "metric": f"context gather rows/s + HBM GB/s & % roofline ({case.cache_dtype} cache -> bf16 rows)",
+        "op": "gather", "impl": "reference", "value": round(v, 3), "unit": "rows/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: whole contexts of {nb} requests per step", "rows": int(cu[-1])},
+        "cpu_baseline": {"value": round(v, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{nb} requests' whole contexts per step x {args.steps} steps"},
+        "e2e": {"value": round(v, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_proj_reference(args):
     """--impl reference --op ...: the oracle's fp64 einsum for the projection,
     timed on the host over K steps of the same inputs as the GPU arm."""
@@ -710,11 +742,7 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.op == "gather":
-        if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "op": "gather",
-                              "unavailable": "the gather's reference arm is its cpu_baseline leg"}), flush=True)
-            return
-        res = run_gather(args)
+        res = run_gather_reference(args) if args.impl == "reference" else run_gather(args)
     elif args.op != "decode":
         res = run_proj_reference(args) if args.impl == "reference" else run_proj(args)
     else:
