@@ -140,6 +140,18 @@ def test_decode_small_head_count(num_heads, sq, num_splits):
     assert mla.decode_status(g.workspace) == 0
 
 
+@pytest.mark.parametrize("num_heads,sq", [(1024, 1), (1000, [2, 1]), (384, 3)])
+def test_decode_large_head_counts(num_heads, sq):
+    """Head counts up to the 1024 the ABI accepts: a token spans several
+    128-row groups, the last one partial when N is not a multiple of 128."""
+    case = synth.make_decode_case(num_heads=num_heads, batch=2, ctx=(100, 600), sq=sq, page_size=64,
+                                  seed=400 + num_heads)
+    g = GpuCase(case)
+    g.decode()
+    compare(case, g, rows=sample_rows(case, 600, seed=num_heads))
+    assert mla.decode_status(g.workspace) == 0
+
+
 def test_decode_negative_scale():
     """A negative softmax scale (the kernel negates q and works with |scale|)."""
     case = synth.make_decode_case(num_heads=16, batch=4, ctx=(60, 500), page_size=64, seed=45)
