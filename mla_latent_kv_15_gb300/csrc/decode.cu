@@ -24,7 +24,9 @@
 //    land in a ring of four receive buffers that needs no return handshake:
 //    a CTA writes tile i+1 into the buffer of tile i-3 only after it has
 //    received tile i-1 from the peer, and the peer sent tile i-1 only after
-//    all its softmax threads had read tile i-3.
+//    all its softmax threads had read tile i-3.  The buffers are chunk-major
+//    ([8 chunks][rows][16 B]), so the 32 lanes of a warp write 512 contiguous
+//    bytes of the peer's shared memory per st.async instruction.
 //  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
 //    bf16 P (A operand of P.V) [464,496).
 //  * Warp roles: a TMA producer, a score-MMA issuer (+TMEM owner), a P.V-MMA
