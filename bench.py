@@ -49,9 +49,16 @@ def peaks():
 
 
 def source_hash(name: str = "decode.cu") -> str:
+    """First 16 hex digits of the sha256 of a kernel source's code: comments
+    and blank lines removed, so that only a change of the code itself makes a
+    recorded profile stale."""
     import hashlib
-    src = os.path.join(ROOT, "mla_latent_kv_15_gb300", "csrc", name)
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    import re
+    text = open(os.path.join(ROOT, "mla_latent_kv_15_gb300", "csrc", name)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", l).rstrip() for l in text.splitlines()]
+    code = "\n".join(l for l in lines if l.strip())
+    return hashlib.sha256(code.encode()).hexdigest()[:16]
 
 
 def profiled_traffic(workload: str, names=None, source: str = "decode.cu"):
@@ -63,7 +70,7 @@ def profiled_traffic(workload: str, names=None, source: str = "decode.cu"):
             continue
         sha, traffic = None, None
         for line in open(path):
-            if "Kernel source sha256" in line:
+            if "Kernel code sha256" in line:
                 sha = line.strip().split()[-1]
             if line.startswith("traffic_bytes_per_launch:"):
                 traffic = int(line.split(":")[1])
