@@ -104,6 +104,17 @@ def f32_to_e4m3(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def quantize_fp8(x_bf16_bits: np.ndarray, scale: float) -> np.ndarray:
+    """scaled_fp8_quant with a static per-tensor scale (common.py,
+    MLACommonImpl.forward, decode branch with an fp8 cache: the absorbed query
+    and q_pe are quantised with layer._q_scale): code = e4m3(float32(x) /
+    float32(scale)), the divide correctly rounded in float32, then the OCP
+    E4M3 encoding (nearest even, finite overflow saturated) -- the same rule
+    as the cache write."""
+    x = bf16_to_f64(np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)).astype(np.float32)
+    return f32_to_e4m3(x / np.float32(scale))
+
+
 # -------------------------------------------------------------- cache write
 
 def cache_write(kv_c: np.ndarray, k_pe: np.ndarray, slot_mapping: np.ndarray, cache: np.ndarray,

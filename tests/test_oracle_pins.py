@@ -430,3 +430,18 @@ def test_gather_e4m3_rounding_matches_torch():
     t = torch.from_numpy(rows).view(torch.float8_e4m3fn).float() * torch.tensor(scale)
     want = t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(got, want)
+
+
+def test_query_quantisation_matches_torch_casts():
+    """scaled_fp8_quant of a bf16 query: float32 divide by the scale, then the
+    e4m3 cast; bit-identical to torch's float32 division and float8_e4m3fn
+    cast (with saturation) on random queries, including values past the
+    range."""
+    rng = np.random.Generator(np.random.PCG64(54))
+    x = rng.standard_normal(20000, dtype=np.float32) * np.float32(3.0)
+    bits = synth.to_bf16_bits(x)
+    scale = float(np.float32(0.0071))
+    got = oracle.quantize_fp8(bits, scale)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float() / torch.tensor(np.float32(scale))
+    want = t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
