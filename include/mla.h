@@ -276,6 +276,20 @@ MLA_API int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_token
 MLA_API int mla_proj_status(int* status, int clear, void* stream);
 
 /*
+ * mla_quantize_fp8 -- scaled_fp8_quant with a static per-tensor scale, as the
+ * decode branch applies it to the absorbed query and q_pe when the cache is
+ * fp8 (common.py, MLACommonImpl.forward: scaled_fp8_quant(..., layer._q_scale)):
+ *
+ *   out[i] = e4m3(float32(x[i]) / float32(scale))
+ *
+ * (float32 divide, round to nearest even, finite overflow saturated to +-448;
+ * the cache write's rule).
+ *   x      [n] bf16, 16-byte aligned;  out [n] e4m3 codes, 8-byte aligned
+ *   scale  finite and > 0;  n >= 0 (0 is a no-op).  One launch.
+ */
+MLA_API int mla_quantize_fp8(const void* x, int64_t n, float scale, void* out, void* stream);
+
+/*
  * mla_gather_cache -- gather_and_maybe_dequant_cache of the chunked-prefill
  * context path (common.py, MLACommonImpl._compute_prefill_context, with the
  * chunk metadata of MLACommonMetadataBuilder): copy the latent rows of a

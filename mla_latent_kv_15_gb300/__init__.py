@@ -29,7 +29,7 @@ DQK = 576
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
                  "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
-                 "mla_gather_cache")
+                 "mla_gather_cache", "mla_quantize_fp8")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -72,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_q_absorb.argtypes = [P, i64, P, i64, i32, i32, P, P]
     lib.mla_v_up_proj.restype = i32
     lib.mla_v_up_proj.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.mla_quantize_fp8.restype = i32
+    lib.mla_quantize_fp8.argtypes = [P, i64, f32, P, P]
     lib.mla_gather_cache.restype = i32
     lib.mla_gather_cache.argtypes = [P, i64, i32, i32, f32, P, i32, P, P, i32, P, i64, P, P]
     lib.mla_proj_status.restype = i32
@@ -187,6 +189,12 @@ def gather_cache(cache, block_table, cu_seq_lens, dst, seq_starts=None, kv_scale
     _check(load().mla_gather_cache(_ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale), _ptr(block_table),
                                    block_table.shape[1], _ptr(cu_seq_lens), _ptr(seq_starts), B, _ptr(dst),
                                    dst.shape[0], _ptr(status), _stream(stream)))
+
+
+def quantize_fp8(x, scale: float, out, stream=None) -> None:
+    """scaled_fp8_quant: out (float8_e4m3fn or uint8, same number of elements)
+    = e4m3(x / scale) for a bf16 tensor x."""
+    _check(load().mla_quantize_fp8(_ptr(x), x.numel(), float(scale), _ptr(out), _stream(stream)))
 
 
 def proj_status(clear: bool = False, stream=None) -> int:

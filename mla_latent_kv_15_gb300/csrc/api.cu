@@ -300,6 +300,17 @@ int mla_gather_cache(const void* cache, int64_t num_blocks, int page_size, int c
   return ok();
 }
 
+int mla_quantize_fp8(const void* x, int64_t n, float scale, void* out, void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n must be >= 0");
+  if (!(std::isfinite(scale) && scale > 0.f)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (n == 0) return ok();
+  if (!x || !out) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(x, 16) || !aligned(out, 8)) return fail(MLA_ERR_INVALID_ARG, "x must be 16-byte and out 8-byte aligned");
+  cudaError_t e = mla::launch_quantize_fp8(x, n, scale, out, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return ok();
+}
+
 int mla_proj_status(int* status, int clear, void* stream) {
   if (!status) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
   cudaError_t e = mla::head_proj_status(status, clear, (cudaStream_t)stream);

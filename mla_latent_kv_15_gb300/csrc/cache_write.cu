@@ -64,7 +64,58 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const __nv_bfloat16* _
   }
 }
 
+// scaled_fp8_quant with a static scale: eight values per thread per step
+// (16-byte load, 8-byte store), grid-stride; a ragged tail element by element.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t n,
+                                                           float scale, uint8_t* __restrict__ out) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t nvec = n / 8;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 src = reinterpret_cast<const uint4*>(x)[v];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&src);
+    float lo[4], hi[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 f0 = __bfloat1622float2(h[k]);
+      const float2 f1 = __bfloat1622float2(h[2 + k]);
+      lo[2 * k] = __fdiv_rn(f0.x, scale);
+      lo[2 * k + 1] = __fdiv_rn(f0.y, scale);
+      hi[2 * k] = __fdiv_rn(f1.x, scale);
+      hi[2 * k + 1] = __fdiv_rn(f1.y, scale);
+    }
+    reinterpret_cast<uint2*>(out)[v] = make_uint2(fp8x4(lo), fp8x4(hi));
+  }
+  const int64_t tail = nvec * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (tail < n && blockIdx.x * (int64_t)blockDim.x + threadIdx.x < 8)
+    out[tail] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(x[tail]), scale), __NV_SATFINITE,
+                                               __NV_E4M3);
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_fp8(const void* x, int64_t n, float scale, void* out, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess || sms <= 0)
+    sms = 148;
+  const int64_t nvec = n / 8;
+  int64_t blocks = (nvec + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_fp8_kernel, static_cast<const __nv_bfloat16*>(x), n, scale,
+                                     static_cast<uint8_t*>(out));
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
                                void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s) {

@@ -140,6 +140,7 @@ size_t decode_smem_bytes(int variant);
 cudaError_t launch_head_proj(const CUtensorMap& tm_x, const CUtensorMap& tm_w, void* y, int64_t T, int N, int d_in,
                              int d_out, cudaStream_t s);
 int head_proj_x_rows(int64_t T);
+cudaError_t launch_quantize_fp8(const void* x, int64_t n, float scale, void* out, cudaStream_t s);
 cudaError_t launch_gather(const void* cache, int64_t num_blocks, int page_size, int cache_fp8, float kv_scale,
                           const int32_t* block_table, int max_pages, const int32_t* cu_seq_lens,
                           const int32_t* seq_starts, int batch, void* dst, int64_t num_tokens, int32_t* status,

@@ -106,6 +106,15 @@ def test_projection_validation_rejects_before_launch(lib):
     assert lib.mla_proj_status(None, 0, None) == -1
 
 
+def test_quantize_validation_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    assert lib.mla_quantize_fp8(P(1 << 20), 10, 0.0, P(1 << 24), None) == -1 and b"scale" in lib.mla_last_error()
+    assert lib.mla_quantize_fp8(P(1 << 20), -1, 1.0, P(1 << 24), None) == -1
+    assert lib.mla_quantize_fp8(P((1 << 20) + 8), 10, 1.0, P(1 << 24), None) == -1
+    assert lib.mla_quantize_fp8(None, 10, 1.0, P(1 << 24), None) == -1
+    assert lib.mla_quantize_fp8(None, 0, 1.0, None, None) == 0
+
+
 def test_gather_validation_rejects_before_launch(lib):
     P = ctypes.c_void_p
     c, bt, cu, d = P(1 << 20), P(1 << 24), P(1 << 26), P(1 << 28)    # never dereferenced

@@ -113,3 +113,16 @@ def test_gather_full_dsv3_contexts():
                                    case.kv_scale, case.block_table, cu, None, int(cu[-1]))
         assert status == 0 and np.array_equal(got, want)
         del g
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 4096 * 128 + 5, 64 * 128 * 576])
+def test_quantize_fp8_bitexact(n):
+    """scaled_fp8_quant on the GPU equals the oracle's float32 divide + e4m3
+    encoding bit for bit (values past the range saturate); ragged lengths."""
+    x = synth.bf16_normal(80 + n % 97, (n,), std=2.0)
+    scale = float(np.float32(3.0 / 448.0))
+    dev = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    out = torch.full((n,), 0x55, dtype=torch.uint8, device="cuda")
+    mla.quantize_fp8(dev, scale, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), oracle.quantize_fp8(x, scale))
