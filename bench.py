@@ -235,8 +235,25 @@ def run_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    fp8q = args.fp8_query
+    if fp8q:
+        if case.cache_dtype != "fp8":
+            raise SystemExit("--fp8-query needs an e4m3-cache workload")
+        # a static per-tensor query scale calibrated on this batch (|q| max / 448)
+        qmax = max(float(np.abs(synth.bf16_bits_to_f32(case.q_abs)).max()),
+                   float(np.abs(synth.bf16_bits_to_f32(case.q_pe)).max()))
+        q_scale = float(np.float32(qmax / 448.0))
+        q8 = torch.empty((T, N, synth.DQK), dtype=torch.uint8, device=dev)
+
     def step(inp, o=out, lo=lse):
         mla.cache_write(inp["kv_c"], inp["k_pe"], inp["slots"], cache, case.kv_scale)
+        if fp8q:
+            # scaled_fp8_quant of q_abs and q_pe into [q_abs | q_pe] rows, then the fp8 x fp8 decode
+            mla.quantize_fp8(inp["q_abs"], q_scale, q8[..., :synth.LKV])
+            mla.quantize_fp8(inp["q_pe"], q_scale, q8[..., synth.LKV:])
+            mla.decode_fp8q(q8, q_scale, cache, inp["block_table"], inp["seq_lens"], o, ws, scale=case.scale,
+                            query_start_loc=inp["qsl"], lse=lo, num_splits=args.num_splits, kv_scale=case.kv_scale)
+            return
         mla.decode(inp["q_abs"], inp["q_pe"], cache, inp["block_table"], inp["seq_lens"], o, ws,
                    scale=case.scale, query_start_loc=inp["qsl"], lse=lo, num_splits=args.num_splits,
                    kv_scale=case.kv_scale)
@@ -330,9 +347,15 @@ def run_gpu(args):
 
     alg = algorithmic(case)
     hbm, tflops, src = peaks()
+    if fp8q:
+        # e4m3 query: one byte per query element; the score FLOPs run on the
+        # fp8 tensor peak (2x the measured bf16 one, the nominal ratio), P.V on bf16
+        alg["decode_bytes"] -= T * N * synth.DQK
+        f_score = alg["flops"] * synth.DQK / (synth.DQK + synth.LKV)
+        tflops = alg["flops"] / (f_score / (2 * tflops) + (alg["flops"] - f_score) / tflops)
     achieved = alg["decode_bytes"] / (kms * 1e-3) / 1e9
     achieved_tf = alg["flops"] / (kms * 1e-3) / 1e12
-    # the binding roof of the workload: bytes at the HBM peak or FLOPs at the bf16 tensor peak
+    # the binding roof of the workload: bytes at the HBM peak or FLOPs at the tensor peak
     hbm_bound = alg["decode_bytes"] / (hbm * 1e9) >= alg["flops"] / (tflops * 1e12)
     traffic = profiled_traffic(args.workload)
     if hbm_bound:
@@ -342,7 +365,8 @@ def run_gpu(args):
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": tflops, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / tflops, 4)}
     roof.update({"traffic": traffic,
-                 "peak_source": f"{src} (MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'})",
+                 "peak_source": f"{src} (MEASURED_PEAKS.json {'hbm_gbs' if hbm_bound else 'bf16_tflops'}"
+                                + (", score FLOPs at 2x for e4m3 x e4m3)" if fp8q and not hbm_bound else ")"),
                  "algorithmic_bytes_per_launch": alg["decode_bytes"], "algorithmic_flops_per_launch": alg["flops"]})
     tok_s = job_throughput(T, world, ms)
     clocks = sampler.summary()
@@ -357,12 +381,13 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if case.cache_dtype == "bf16" else "e4m3-cache/bf16",
+        "dtype": "bf16" if case.cache_dtype == "bf16" else ("e4m3 q,k / bf16 p,v" if fp8q else "e4m3-cache/bf16"),
         "data": "synthetic",
         "config": {
             "workload": args.workload, "num_heads": N, "batch": B, "total_q": T,
             "ctx_sum": int(case.seq_lens.sum()), "page_size": case.page_size, "num_blocks": case.num_blocks,
-            "cache_dtype": case.cache_dtype, "num_splits": args.num_splits, "parallelism": f"replicas{world}",
+            "cache_dtype": case.cache_dtype, "query": "e4m3 (scaled_fp8_quant each step)" if fp8q else "bf16",
+            "num_splits": args.num_splits, "parallelism": f"replicas{world}",
             "l2": "flushed (256 MiB write) before every timed step",
             "timing": "value: K whole steps, CUDA events per step; roofline: a second pass of K steps "
                       "with events around the decode kernel",
@@ -744,6 +769,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8-query", action="store_true",
+                    help="e4m3 workloads: quantise the query each step and run the fp8 x fp8 decode")
     ap.add_argument("--op", default="decode", choices=["decode", "q_absorb", "v_up_proj", "gather"])
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

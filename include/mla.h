@@ -276,18 +276,43 @@ MLA_API int mla_v_up_proj(const void* o_lat, const void* w_uv, int64_t num_token
 MLA_API int mla_proj_status(int* status, int clear, void* stream);
 
 /*
+ * mla_decode_fp8q -- mla_decode with an e4m3 query over an e4m3 cache: the
+ * decode branch's fp8 path (common.py, MLACommonImpl.forward: with an fp8
+ * cache the absorbed query and q_pe are quantised by scaled_fp8_quant with
+ * layer._q_scale, and the kernels get q_scale and k_scale; the scores'
+ * factor is scale * q_scale * k_scale, as FlashInferImpl.get_xqa_bmm1_scale
+ * forms it).  The score products run on the fp8 tensor cores (e4m3 x e4m3,
+ * float32 accumulation); P.V stays bf16 x bf16 (values expanded exactly).
+ *   q_fp8     [total_q, num_heads, 576] e4m3 codes, rows [q_abs | q_pe]
+ *             quantised with q_scale (mla_quantize_fp8), 16-byte aligned
+ *   q_scale   finite and > 0
+ *   the cache must be e4m3 (kv_scale finite and > 0); every other argument,
+ *   the output, the LSE, the workspace and the error behaviour are those of
+ *   mla_decode.
+ */
+MLA_API int mla_decode_fp8q(const void* q_fp8, float q_scale, const void* cache, int64_t num_blocks, int page_size,
+                            float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+                            const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q,
+                            int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * mla_quantize_fp8 -- scaled_fp8_quant with a static per-tensor scale, as the
  * decode branch applies it to the absorbed query and q_pe when the cache is
  * fp8 (common.py, MLACommonImpl.forward: scaled_fp8_quant(..., layer._q_scale)):
  *
- *   out[i] = e4m3(float32(x[i]) / float32(scale))
+ *   out[r * out_stride + c] = e4m3(float32(x[r * x_stride + c]) / float32(scale))
  *
- * (float32 divide, round to nearest even, finite overflow saturated to +-448;
- * the cache write's rule).
- *   x      [n] bf16, 16-byte aligned;  out [n] e4m3 codes, 8-byte aligned
- *   scale  finite and > 0;  n >= 0 (0 is a no-op).  One launch.
+ * for r < rows, c < width (float32 divide, round to nearest even, finite
+ * overflow saturated to +-448; the cache write's rule).  The strides let
+ * q_abs and q_pe go straight into the [q_abs | q_pe] rows mla_decode_fp8q reads.
+ *   x      bf16, 16-byte aligned, x_stride (elements) a multiple of 8
+ *   out    e4m3 codes, 8-byte aligned, out_stride (elements) a multiple of 8
+ *   width  a multiple of 8, <= both strides;  rows >= 0 (0 is a no-op)
+ *   scale  finite and > 0.  One launch.
  */
-MLA_API int mla_quantize_fp8(const void* x, int64_t n, float scale, void* out, void* stream);
+MLA_API int mla_quantize_fp8(const void* x, int64_t x_stride, int64_t rows, int width, float scale, void* out,
+                             int64_t out_stride, void* stream);
 
 /*
  * mla_gather_cache -- gather_and_maybe_dequant_cache of the chunked-prefill

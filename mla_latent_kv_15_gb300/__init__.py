@@ -29,7 +29,7 @@ DQK = 576
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
                  "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
-                 "mla_gather_cache", "mla_quantize_fp8")
+                 "mla_gather_cache", "mla_quantize_fp8", "mla_decode_fp8q")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -72,8 +72,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_q_absorb.argtypes = [P, i64, P, i64, i32, i32, P, P]
     lib.mla_v_up_proj.restype = i32
     lib.mla_v_up_proj.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.mla_decode_fp8q.restype = i32
+    lib.mla_decode_fp8q.argtypes = [P, f32, P, i64, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32, P, P, P, sz, P]
     lib.mla_quantize_fp8.restype = i32
-    lib.mla_quantize_fp8.argtypes = [P, i64, f32, P, P]
+    lib.mla_quantize_fp8.argtypes = [P, i64, i64, i32, f32, P, i64, P]
     lib.mla_gather_cache.restype = i32
     lib.mla_gather_cache.argtypes = [P, i64, i32, i32, f32, P, i32, P, P, i32, P, i64, P, P]
     lib.mla_proj_status.restype = i32
@@ -145,6 +147,19 @@ def decode_no_alloc(q_abs, q_pe, cache, block_table, seq_lens, out, *, scale: fl
                                       _ptr(lse), _stream(stream)))
 
 
+def decode_fp8q(q_fp8, q_scale: float, cache, block_table, seq_lens, out, workspace, *, scale: float,
+                query_start_loc=None, lse=None, num_splits: int = 0, kv_scale: float = 1.0, stream=None) -> None:
+    """decode() with an e4m3 query ``q_fp8`` [T, N, 576] (quantised with
+    q_scale) over an e4m3 cache: fp8 x fp8 score MMAs."""
+    T, N, _ = q_fp8.shape
+    nb, ps, _ = cache.shape
+    B = seq_lens.numel()
+    _check(load().mla_decode_fp8q(_ptr(q_fp8), float(q_scale), _ptr(cache), nb, ps, float(kv_scale),
+                                  _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
+                                  T, N, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def decode_status(workspace, stream=None) -> int:
     st = ctypes.c_int(0)
     _check(load().mla_decode_status(_ptr(workspace), ctypes.byref(st), _stream(stream)))
@@ -192,9 +207,32 @@ def gather_cache(cache, block_table, cu_seq_lens, dst, seq_starts=None, kv_scale
 
 
 def quantize_fp8(x, scale: float, out, stream=None) -> None:
-    """scaled_fp8_quant: out (float8_e4m3fn or uint8, same number of elements)
-    = e4m3(x / scale) for a bf16 tensor x."""
-    _check(load().mla_quantize_fp8(_ptr(x), x.numel(), float(scale), _ptr(out), _stream(stream)))
+    """scaled_fp8_quant: out = e4m3(x / scale) row by row.  ``x`` (bf16) and
+    ``out`` (uint8 or float8_e4m3fn) have the same shape; their last dimension
+    is contiguous and may be a column slice of wider rows (e.g. the q_abs and
+    q_pe parts of [q_abs | q_pe] rows); 1-D tensors are one row."""
+    if tuple(x.shape) != tuple(out.shape):
+        raise ValueError("x and out must have the same shape")
+    width = x.shape[-1]
+    rows = x.numel() // width if width else 0
+    xs, os_ = _row_pitch(x), _row_pitch(out)
+    _check(load().mla_quantize_fp8(_ptr(x), xs, rows, width, float(scale), _ptr(out), os_, _stream(stream)))
+
+
+def _row_pitch(t) -> int:
+    """Element distance between consecutive rows (last dimension = a row) of
+    a tensor whose rows are equally spaced with a contiguous last dimension."""
+    if t.dim() == 1:
+        return t.numel()
+    if t.stride(-1) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    pitch = t.stride(-2)
+    expect = pitch
+    for d in range(t.dim() - 2, -1, -1):
+        if t.shape[d] > 1 and t.stride(d) != expect:
+            raise ValueError("rows must be equally spaced")
+        expect *= t.shape[d]
+    return pitch
 
 
 def proj_status(clear: bool = False, stream=None) -> int:

@@ -96,20 +96,31 @@ size_t mla_decode_workspace_size(int batch, int total_q, int num_heads, int max_
   return mla::workspace_layout(batch, total_q, num_heads, max_splits).total;
 }
 
-int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks, int page_size,
-               int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
-               const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q, int num_heads,
-               float scale, int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
-               void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The decode of mla_decode (q8 == nullptr: bf16 q_abs and q_pe) and of
+// mla_decode_fp8q (q8: e4m3 [q_abs | q_pe] rows with q_scale, e4m3 cache).
+int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_scale, const void* cache,
+                int64_t num_blocks, int page_size, int cache_dtype, float kv_scale, const int32_t* block_table,
+                int max_pages_per_seq, const int32_t* seq_lens, int batch, const int32_t* query_start_loc,
+                int total_q, int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
   if (batch < 0 || total_q < 0) return fail(MLA_ERR_INVALID_ARG, "batch and total_q must be >= 0");
   if (num_heads < 1 || num_heads > 1024) return fail(MLA_ERR_INVALID_ARG, "num_heads must be in [1, 1024]");
   if (batch == 0 || total_q == 0) return ok();
   if (!query_start_loc && total_q != batch)
     return fail(MLA_ERR_INVALID_ARG, "without query_start_loc every request has one query token (total_q == batch)");
-  if (!q_abs || !q_pe || !cache || !block_table || !seq_lens || !out || !workspace)
+  if ((q8 ? !q8 : (!q_abs || !q_pe)) || !cache || !block_table || !seq_lens || !out || !workspace)
     return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned(q_abs, 16) || !aligned(q_pe, 16) || !aligned(cache, 16) || !aligned(out, 16))
-    return fail(MLA_ERR_INVALID_ARG, "q_abs, q_pe, cache and out must be 16-byte aligned");
+  if ((q8 ? !aligned(q8, 16) : (!aligned(q_abs, 16) || !aligned(q_pe, 16))) || !aligned(cache, 16) ||
+      !aligned(out, 16))
+    return fail(MLA_ERR_INVALID_ARG, "the query, cache and out must be 16-byte aligned");
+  if (q8 && cache_dtype != MLA_FP8_E4M3)
+    return fail(MLA_ERR_UNSUPPORTED, "an e4m3 query needs an e4m3 cache");
+  if (q8 && !(std::isfinite(q_scale) && q_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "q_scale must be finite and > 0");
   if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (query_start_loc && !aligned(query_start_loc, 4)) ||
       (lse && !aligned(lse, 4)))
     return fail(MLA_ERR_INVALID_ARG, "block_table, seq_lens, query_start_loc and lse must be 4-byte aligned");
@@ -138,8 +149,17 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   const uint64_t rows = (uint64_t)total_q * num_heads;
   CUtensorMap tm_q, tm_qpe, tm_kv;
   const uint32_t kv_box_rows = page_size < mla::kTile ? page_size : mla::kTile;
-  if (!mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64, 64,
-                           CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (q8) {
+    // e4m3 query rows and cache rows (576 wide) in 128-dim, 128-byte-swizzled boxes
+    if (!mla::encode_tmap_2d(&tm_q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, rows, mla::kDqk, 128, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk,
+                             (uint64_t)num_blocks * page_size, mla::kDqk, 128, kv_box_rows,
+                             CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
+    tm_qpe = tm_q;   // not read by the e4m3-query kernel
+  } else if (!mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64,
+                                  64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !mla::encode_tmap_2d(&tm_qpe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 64, 64,
                            CU_TENSOR_MAP_SWIZZLE_128B) ||
       !(cache_dtype == MLA_BF16
@@ -165,6 +185,12 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   const float kvs = cache_dtype == MLA_FP8_E4M3 ? kv_scale : 1.f;
   // the kernel works with a positive scale; a negative one negates q instead
   a.scale_log2 = std::fabs(scale) * 1.4426950408889634f * kvs;
+  if (q8) {
+    // the e4m3-query kernel turns its code-product sums into real partial
+    // scores (x q_scale x kv_scale) before the exchange
+    a.qk_scale = q_scale * kv_scale;
+    a.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  }
   a.neg_q = scale < 0.f;
   a.out_scale = kvs;
   a.out = out;
@@ -176,18 +202,42 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   // 32-row groups and the decode variant with small receive buffers and a
   // deeper cache ring.  Groups never outnumber the batch then: a request with
   // Sq tokens gives ceil(Sq * N / 32) <= Sq groups.
-  const int small_rows = cache_dtype == MLA_BF16 && num_heads <= 32 && total_q == batch;
+  const int small_rows = !q8 && cache_dtype == MLA_BF16 && num_heads <= 32 && total_q == batch;
+  const int variant = q8 ? 3 : (cache_dtype == MLA_FP8_E4M3 ? 1 : (small_rows ? 2 : 0));
   cudaError_t e = mla::launch_plan(seq_lens, query_start_loc, batch, num_heads, max_pages_per_seq, page_size,
                                    num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
-  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, cache_dtype, small_rows, a, clusters, s);
+  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, variant, a, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
   e = mla::launch_combine(a, L.max_groups, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks, int page_size,
+               int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+               const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q, int num_heads,
+               float scale, int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  return decode_impl(q_abs, q_pe, nullptr, 0.f, cache, num_blocks, page_size, cache_dtype, kv_scale, block_table,
+                     max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale, num_splits, out,
+                     lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_fp8q(const void* q_fp8, float q_scale, const void* cache, int64_t num_blocks, int page_size,
+                    float kv_scale, const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                    int batch, const int32_t* query_start_loc, int total_q, int num_heads, float scale,
+                    int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(nullptr, nullptr, q_fp8, q_scale, cache, num_blocks, page_size, MLA_FP8_E4M3, kv_scale,
+                     block_table, max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale,
+                     num_splits, out, lse, workspace, workspace_bytes, stream);
 }
 
 int mla_decode_status(const void* workspace, int* status, void* stream) {
@@ -300,13 +350,17 @@ int mla_gather_cache(const void* cache, int64_t num_blocks, int page_size, int c
   return ok();
 }
 
-int mla_quantize_fp8(const void* x, int64_t n, float scale, void* out, void* stream) {
-  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n must be >= 0");
+int mla_quantize_fp8(const void* x, int64_t x_stride, int64_t rows, int width, float scale, void* out,
+                     int64_t out_stride, void* stream) {
+  if (rows < 0) return fail(MLA_ERR_INVALID_ARG, "rows must be >= 0");
+  if (width <= 0 || width % 8 != 0) return fail(MLA_ERR_INVALID_ARG, "width must be a positive multiple of 8");
+  if (x_stride < width || x_stride % 8 != 0 || out_stride < width || out_stride % 8 != 0)
+    return fail(MLA_ERR_INVALID_ARG, "strides must be multiples of 8 and at least width");
   if (!(std::isfinite(scale) && scale > 0.f)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (n == 0) return ok();
+  if (rows == 0) return ok();
   if (!x || !out) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned(x, 16) || !aligned(out, 8)) return fail(MLA_ERR_INVALID_ARG, "x must be 16-byte and out 8-byte aligned");
-  cudaError_t e = mla::launch_quantize_fp8(x, n, scale, out, (cudaStream_t)stream);
+  cudaError_t e = mla::launch_quantize_fp8(x, x_stride, rows, width, scale, out, out_stride, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return ok();
 }

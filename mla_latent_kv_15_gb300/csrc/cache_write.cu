@@ -64,14 +64,20 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const __nv_bfloat16* _
   }
 }
 
-// scaled_fp8_quant with a static scale: eight values per thread per step
-// (16-byte load, 8-byte store), grid-stride; a ragged tail element by element.
-__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t n,
-                                                           float scale, uint8_t* __restrict__ out) {
+// scaled_fp8_quant with a static scale over `rows` rows of `width` values
+// (width a multiple of 8; row pitches in elements, multiples of 8 for x and
+// of 8 for out): eight values per thread per step (16-byte load, 8-byte
+// store), grid-stride.
+__global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
+                                                           int64_t rows, int width, float scale,
+                                                           uint8_t* __restrict__ out, int64_t out_stride) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t nvec = n / 8;
+  const int vpr = width / 8;
+  const int64_t nvec = rows * vpr;
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 src = reinterpret_cast<const uint4*>(x)[v];
+    const int64_t r = v / vpr;
+    const int c = (int)(v - r * vpr) * 8;
+    const uint4 src = *reinterpret_cast<const uint4*>(x + r * x_stride + c);
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&src);
     float lo[4], hi[4];
 #pragma unroll
@@ -83,22 +89,19 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
       hi[2 * k] = __fdiv_rn(f1.x, scale);
       hi[2 * k + 1] = __fdiv_rn(f1.y, scale);
     }
-    reinterpret_cast<uint2*>(out)[v] = make_uint2(fp8x4(lo), fp8x4(hi));
+    *reinterpret_cast<uint2*>(out + r * out_stride + c) = make_uint2(fp8x4(lo), fp8x4(hi));
   }
-  const int64_t tail = nvec * 8 + blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (tail < n && blockIdx.x * (int64_t)blockDim.x + threadIdx.x < 8)
-    out[tail] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(__bfloat162float(x[tail]), scale), __NV_SATFINITE,
-                                               __NV_E4M3);
 }
 
 }  // namespace
 
-cudaError_t launch_quantize_fp8(const void* x, int64_t n, float scale, void* out, cudaStream_t s) {
+cudaError_t launch_quantize_fp8(const void* x, int64_t x_stride, int64_t rows, int width, float scale, void* out,
+                                int64_t out_stride, cudaStream_t s) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                 cudaSuccess || sms <= 0)
     sms = 148;
-  const int64_t nvec = n / 8;
+  const int64_t nvec = rows * (width / 8);
   int64_t blocks = (nvec + 255) / 256;
   if (blocks < 1) blocks = 1;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
@@ -111,8 +114,8 @@ cudaError_t launch_quantize_fp8(const void* x, int64_t n, float scale, void* out
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_fp8_kernel, static_cast<const __nv_bfloat16*>(x), n, scale,
-                                     static_cast<uint8_t*>(out));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_fp8_kernel, static_cast<const __nv_bfloat16*>(x), x_stride, rows,
+                                     width, scale, static_cast<uint8_t*>(out), out_stride);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

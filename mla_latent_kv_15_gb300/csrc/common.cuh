@@ -115,6 +115,7 @@ struct DecodeArgs {
   float scale_log2;         // |scale| * log2(e) (* kv_scale for fp8), > 0
   int neg_q;                // scale < 0: the kernel negates the query instead
   float out_scale;          // kv_scale for fp8, 1 for bf16
+  float qk_scale;           // e4m3 query: q_scale * kv_scale (code products -> scores)
   void* out;                // bf16 [T*N, 512]
   float* lse;               // [T*N] or null
   Plan plan;
@@ -124,9 +125,10 @@ struct DecodeArgs {
 // group_rows: query rows per group (128; 32 for the small-rows decode variant)
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s);
-// small_rows: bf16 cache and every group has at most 32 rows (plan built with group_rows = 32)
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
-                          int cache_dtype, int small_rows, const DecodeArgs& a, int num_clusters, cudaStream_t s);
+// variant: 0 bf16 cache, 1 e4m3 cache, 2 bf16 cache with <= 32-row groups
+// (plan built with group_rows = 32), 3 e4m3 query and e4m3 cache
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv, int variant,
+                          const DecodeArgs& a, int num_clusters, cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                                 int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,
@@ -140,7 +142,8 @@ size_t decode_smem_bytes(int variant);
 cudaError_t launch_head_proj(const CUtensorMap& tm_x, const CUtensorMap& tm_w, void* y, int64_t T, int N, int d_in,
                              int d_out, cudaStream_t s);
 int head_proj_x_rows(int64_t T);
-cudaError_t launch_quantize_fp8(const void* x, int64_t n, float scale, void* out, cudaStream_t s);
+cudaError_t launch_quantize_fp8(const void* x, int64_t x_stride, int64_t rows, int width, float scale, void* out,
+                                int64_t out_stride, cudaStream_t s);
 cudaError_t launch_gather(const void* cache, int64_t num_blocks, int page_size, int cache_fp8, float kv_scale,
                           const int32_t* block_table, int max_pages, const int32_t* cu_seq_lens,
                           const int32_t* seq_starts, int batch, void* dst, int64_t num_tokens, int32_t* status,

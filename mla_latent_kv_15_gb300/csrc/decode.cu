@@ -62,8 +62,18 @@ constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B row
 constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
 // An e4m3 tile lands in the upper half of the bf16 stage it is expanded into.
 constexpr int kFp8InPlace = kStageBytes - kFp8TileBytes;
+// e4m3 query and cache (variant 3): each item lands as three 128-dim boxes
+// (64 rows x 128 e4m3, 128-B swizzle) that the fp8 score MMAs read directly,
+// in the top 24 KB of the slot; the value dims are then expanded to bf16
+// below them (boxes 0-3 of the slot), once the score MMAs are done.
+constexpr int kQ8Box = 64 * 128;
+constexpr int kQ8Boxes = 3;
+constexpr int kQ8Bytes = kQ8Boxes * kQ8Box;
+constexpr int kQ8InPlace = kStageBytes - kQ8Bytes;
+static_assert(kQ8InPlace % 1024 == 0 && kQ8InPlace + kQ8Bytes == kStageBytes, "e4m3 landing area");
 // Kernel variants: 0 bf16 cache; 1 e4m3 cache (expanded in place in the bf16
-// ring); 2 bf16 cache with at most 32
+// ring); 3 e4m3 query and e4m3 cache (fp8 score MMAs, values expanded for
+// P.V); 2 bf16 cache with at most 32
 // query rows per unit (small head counts: the receive ring shrinks to 32-row
 // buffers and the cache ring gets a fifth stage).
 template <int kVariant>
@@ -108,6 +118,7 @@ struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];  // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
   uint64_t stg_full[kMaxStages];  // e4m3 tile landed in the upper half of its ring slot
+  uint64_t kx_free[kMaxStages];   // variant 3: the slot's score MMAs are done (its e4m3 boxes may be overwritten)
   uint64_t q_ready;
   uint64_t s_full;
   uint64_t s_free;
@@ -126,7 +137,8 @@ constexpr size_t smem_bytes() {
   return 1024 + (size_t)Layout<kVariant>::kStages * kStageBytes +
          kXBuffers * (size_t)Layout<kVariant>::kXBytes + sizeof(Barriers);
 }
-static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
+static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
+                  smem_bytes<3>() <= 232448,
               "shared memory per CTA");
 static_assert(Layout<0>::kStages <= kMaxStages && Layout<1>::kStages <= kMaxStages && Layout<2>::kStages <= kMaxStages,
               "barrier arrays");
@@ -214,6 +226,11 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
 __device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
   return rank == 0 ? (p < 4 || k < 2) : (p > 0 || k >= 2);
 }
+// Variant 3: 32-dim K steps of the three 128-dim e4m3 boxes.  CTA 0 (dims
+// 0-383 loaded) uses dims 0-287; CTA 1 (dims 256-639 loaded) uses 288-575.
+__device__ __forceinline__ constexpr bool kstep8_valid(uint32_t rank, int p, int k) {
+  return rank == 0 ? (p < 2 || k == 0) : (p == 1 || (p == 0 && k >= 1) || (p == 2 && k < 2));
+}
 
 // Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major, in the upper
 // half of the ring slot) into the bf16 128-byte-swizzled layout the MMAs read
@@ -253,10 +270,11 @@ __device__ __forceinline__ void expand_e4m3_tile(uint32_t stage, int t) {
 }
 
 template <int kVariant>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 || kVariant == 3>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
                   const __grid_constant__ CUtensorMap tm_kv, const DecodeArgs a) {
-  constexpr int kCacheFp8 = kVariant == 1;
+  constexpr int kCacheFp8 = kVariant == 1 || kVariant == 3;
+  constexpr bool kQ8 = kVariant == 3;       // e4m3 query: fp8 x fp8 score MMAs
   constexpr int kStages = Layout<kVariant>::kStages;
   constexpr int kXBytes = Layout<kVariant>::kXBytes;
   constexpr int kXRows = Layout<kVariant>::kXRows;
@@ -279,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       mbar_init(smem_u32(&bars->kv_empty[i]), 2);
     }
     for (int i = 0; i < kMaxStages; ++i) mbar_init(smem_u32(&bars->stg_full[i]), 1);
+    for (int i = 0; i < kMaxStages; ++i) mbar_init(smem_u32(&bars->kx_free[i]), 1);
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
     mbar_init(smem_u32(&bars->s_free), 4);
@@ -347,6 +366,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
               tma_load_2d(dst + p * box_bytes + sb * sub_rows * row_bytes, &tm_kv, 256 * rank + 64 * p, y, full);
           }
         };
+        // variant 3: the CTA's three 128-dim e4m3 boxes of tile j (128-B swizzle)
+        auto load_tile8 = [&](int j, uint32_t dst, uint32_t full) {
+          for (int sb = 0; sb < nsub; ++sb) {
+            const int key = j * kTile + sb * sub_rows;
+            const int lp = key / a.page_size;
+            int y = oob_row;
+            if (key < gr.lmax && lp < a.max_pages) {
+              const int blk = bt[lp];
+              if (blk >= 0 && blk < a.num_blocks)
+                y = blk * a.page_size + key % a.page_size;
+              else
+                atomicOr(ctx.status, 4);
+            }
+            for (int p = 0; p < kQ8Boxes; ++p)
+              tma_load_2d(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, 256 * rank + 128 * p, y, full);
+          }
+        };
         const int ntiles = ur.tile_end - ur.tile_begin;
         // the CTA's 288 query dims (5 boxes of 64) for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
@@ -354,18 +390,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
           const uint32_t slot = item % kStages, round = item / kStages;
           wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
-          const uint32_t full = smem_u32(&bars->kv_full[slot]);
-          mbar_expect_tx(full, kStageBytes);
           const int y = gr.row0 + 64 * half;
-          for (int p = 0; p < kBoxesPerStage; ++p) {
-            if (rank == 1 && p == 4)
-              tma_load_2d(st + p * kBox, &tm_qpe, 0, y, full);
-            else
-              tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
+          if constexpr (kQ8) {
+            // e4m3 query rows [q_abs | q_pe] (576 wide): the CTA's three
+            // 128-dim boxes; the last box of CTA 1 runs past dim 575 (zeros)
+            const uint32_t full = smem_u32(&bars->stg_full[slot]);
+            mbar_expect_tx(full, kQ8Bytes);
+            for (int p = 0; p < kQ8Boxes; ++p)
+              tma_load_2d(st + kQ8InPlace + p * kQ8Box, &tm_q, 256 * rank + 128 * p, y, full);
+            // kv_full's phases count every item of the slot
+            mbar_arrive(smem_u32(&bars->kv_full[slot]));
+          } else {
+            const uint32_t full = smem_u32(&bars->kv_full[slot]);
+            mbar_expect_tx(full, kStageBytes);
+            for (int p = 0; p < kBoxesPerStage; ++p) {
+              if (rank == 1 && p == 4)
+                tma_load_2d(st + p * kBox, &tm_qpe, 0, y, full);
+              else
+                tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
+            }
+            // e4m3 cache: a query item also completes a phase of the slot's
+            // stg_full, so its phases count every item of the slot
+            if (kCacheFp8) mbar_arrive(smem_u32(&bars->stg_full[slot]));
           }
-          // e4m3 cache: a query item also completes a phase of the slot's
-          // stg_full, so its phases count every item of the slot
-          if (kCacheFp8) mbar_arrive(smem_u32(&bars->stg_full[slot]));
         }
         for (int jj = 0; jj < ntiles; ++jj, ++item) {
           const uint32_t slot = item % kStages, round = item / kStages;
@@ -374,6 +421,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
             const uint32_t full = smem_u32(&bars->kv_full[slot]);
             mbar_expect_tx(full, kStageBytes);
             load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full, 128);
+          } else if constexpr (kQ8) {
+            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+            const uint32_t full = smem_u32(&bars->stg_full[slot]);
+            mbar_expect_tx(full, kQ8Bytes);
+            load_tile8(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kQ8InPlace), full);
           } else {
             wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
             const uint32_t full = smem_u32(&bars->stg_full[slot]);
@@ -382,10 +434,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
           }
         }
       }
-      // drain: every issued load has landed before the CTA may exit
+      // drain: every issued load has landed before the CTA may exit (with an
+      // e4m3 query every item's loads complete on stg_full)
       if (leader) {
         const uint32_t first = item > kStages ? item - kStages : 0;
-        for (uint32_t k = first; k < item; ++k) mbar_wait(smem_u32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
+        for (uint32_t k = first; k < item; ++k)
+          mbar_wait(smem_u32(kQ8 ? &bars->stg_full[k % kStages] : &bars->kv_full[k % kStages]), (k / kStages) & 1);
       }
     }
     __syncwarp();
@@ -404,8 +458,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
         const int ntiles = ur.tile_end - ur.tile_begin;
         item += 2;  // query items are consumed by the softmax warps
         wait_bar(ctx, &bars->q_ready, units_done & 1);
+        if constexpr (kQ8) {
+          // the query items' slots get their kx_free phase too (after every
+          // earlier MMA, like the tile items' commits)
+          mma_commit(smem_u32(&bars->kx_free[(item - 2) % kStages]));
+          mma_commit(smem_u32(&bars->kx_free[(item - 1) % kStages]));
+        }
         for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
           const uint32_t slot = item % kStages, round = item / kStages;
+          if constexpr (kQ8) {
+            // fp8 x fp8: the e4m3 boxes are read as they landed, 9 MMAs of K = 32
+            wait_bar(ctx, &bars->stg_full[slot], round & 1);
+            wait_bar(ctx, &bars->s_free, (it & 1) ^ 1);
+            tc_fence_after();
+            constexpr uint32_t id_s8 = idesc_e4m3_f32(128, kTile);
+            const uint64_t kd8 = smem_desc(smem_u32(stages + slot * kStageBytes + kQ8InPlace), 16, 1024, kSwizzle128B);
+            uint32_t j = 0;
+#pragma unroll
+            for (int p = 0; p < kQ8Boxes; ++p)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (kstep8_valid(rank, p, k)) {
+                  mma_ts_f8(d, tbase + kTmemQ + 8 * j, kd8 + ((p * kQ8Box + k * 32) >> 4), id_s8, j > 0 ? 1u : 0u);
+                  ++j;
+                }
+            mma_commit(smem_u32(&bars->s_full));
+            mma_commit(smem_u32(&bars->kv_empty[slot]));
+            mma_commit(smem_u32(&bars->kx_free[slot]));
+            continue;
+          }
           wait_bar(ctx, &bars->kv_full[slot], round & 1);
           wait_bar(ctx, &bars->s_free, (it & 1) ^ 1);
           tc_fence_after();
@@ -471,7 +552,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       for (int jj = 0; jj < ntiles; ++jj, ++item) {
         const uint32_t slot = item % kStages, round = item / kStages;
         wait_bar(ctx, &bars->stg_full[slot], round & 1);
-        expand_e4m3_tile(smem_u32(stages + slot * kStageBytes), te);
+        if constexpr (kQ8) {
+          // Variant 3: the value dims (e4m3 boxes 0-1 = the CTA's 256 output
+          // dims) become the bf16 boxes 0-3 of the slot, which overlap e4m3
+          // boxes 0-1: read everything, wait until the tile's score MMAs are
+          // done with the e4m3 boxes, then write.
+          const uint32_t st = smem_u32(stages + slot * kStageBytes);
+          uint4 v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = te + 128 * k;
+            const int q = i & 7, r = (i >> 3) & 63, b = i >> 9;   // 16-byte chunk, row (key), e4m3 box
+            v[k] = lds128(st + kQ8InPlace + b * kQ8Box + r * 128 + ((q ^ (r & 7)) << 4));
+          }
+          wait_bar(ctx, &bars->kx_free[slot], round & 1);
+          named_bar_expand();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int i = te + 128 * k;
+            const int q = i & 7, r = (i >> 3) & 63, b = i >> 9;
+            // 16 values: output dims 128 b + 16 q + [0, 16) -> bf16 box 2b + q/4, chunks 2(q%4), 2(q%4)+1
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] & 0xFFFF), __NV_E4M3);
+              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] >> 16), __NV_E4M3);
+              const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+              const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+              o[2 * j] = pack_bf16x2(flo.x, flo.y);
+              o[2 * j + 1] = pack_bf16x2(fhi.x, fhi.y);
+            }
+            const uint32_t rowa = st + (2 * b + (q >> 2)) * kBox + r * 128;
+            const int c0 = 2 * (q & 3);
+            sts128(rowa + ((c0 ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
+            sts128(rowa + (((c0 + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
+          }
+        } else {
+          expand_e4m3_tile(smem_u32(stages + slot * kStageBytes), te);
+        }
         fence_proxy_async_smem();    // bf16 writes visible to the MMAs
         named_bar_expand();
         if (te == 0) {
@@ -510,6 +629,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       for (int c = 0; c < 32; ++c) {
         dst[c] = __uint_as_float(r0[c]);
         dst[32 + c] = __uint_as_float(r1[c]);
+      }
+      if constexpr (kQ8) {
+        // sums of code products -> real partial scores before the fp16 exchange
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) dst[c] *= a.qk_scale;
       }
       tc_fence_before();
       __syncwarp();
@@ -576,7 +700,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
       const uint32_t nbytes = (uint32_t)gr.nrows * (kTile * 2);
 
       // the CTA's 288 query dims -> TMEM (A operand of the score MMAs)
-      {
+      if constexpr (kQ8) {
+        // e4m3 query: the nine 32-dim K steps of the CTA's 288 dims, four
+        // codes per TMEM column, in the order the score issuer walks them
+        const uint32_t my = item + (row >= 64 ? 1 : 0);
+        wait_bar(ctx, &bars->stg_full[my % kStages], (my / kStages) & 1);
+        __syncwarp();
+        const int k = row & 63;
+        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + kQ8InPlace + k * 128;
+        const uint32_t sgn = a.neg_q ? 0x80808080u : 0u;   // a negative scale negates q
+        uint32_t j = 0;
+#pragma unroll
+        for (int p = 0; p < kQ8Boxes; ++p)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            if (kstep8_valid(rank, p, kk)) {
+              const uint4 v0 = lds128(base + p * kQ8Box + (((2 * kk) ^ (k & 7)) << 4));
+              const uint4 v1 = lds128(base + p * kQ8Box + (((2 * kk + 1) ^ (k & 7)) << 4));
+              const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
+                                     v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
+              tmem_st8(tl + kTmemQ + 8 * j, w);
+              ++j;
+            }
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_softmax();
+        if (tid128 == 0) {
+          for (int qi = 0; qi < 2; ++qi) {      // two arrivals: the slot's count covers both issuers
+            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+          }
+          mbar_arrive(smem_u32(&bars->q_ready));
+        }
+        item += 2;
+      } else {
         const uint32_t my = item + (row >= 64 ? 1 : 0);
         wait_bar(ctx, &bars->kv_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
@@ -793,21 +950,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1>
 }  // namespace
 
 size_t decode_smem_bytes(int variant) {
-  return variant == 1 ? smem_bytes<1>() : (variant == 2 ? smem_bytes<2>() : smem_bytes<0>());
+  return variant == 1 ? smem_bytes<1>()
+                      : (variant == 2 ? smem_bytes<2>() : (variant == 3 ? smem_bytes<3>() : smem_bytes<0>()));
 }
 
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv,
-                          int cache_dtype, int small_rows, const DecodeArgs& a, int num_clusters, cudaStream_t s) {
-  const int variant = cache_dtype ? 1 : (small_rows ? 2 : 0);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv, int variant,
+                          const DecodeArgs& a, int num_clusters, cudaStream_t s) {
   const size_t smem = decode_smem_bytes(variant);
-  auto kern = variant == 1 ? decode_kernel<1> : (variant == 2 ? decode_kernel<2> : decode_kernel<0>);
+  auto kern = variant == 1 ? decode_kernel<1>
+                           : (variant == 2 ? decode_kernel<2> : (variant == 3 ? decode_kernel<3> : decode_kernel<0>));
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the prologue (barriers, TMEM, cluster
   // sync) overlaps the plan kernel; the kernel waits for it before reading the plan
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
-  cfg.blockDim = dim3(variant == 1 ? Roles<1>::kThreads : Roles<0>::kThreads);
+  cfg.blockDim = dim3(variant == 1 || variant == 3 ? Roles<1>::kThreads : Roles<0>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

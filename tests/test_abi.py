@@ -108,11 +108,14 @@ def test_projection_validation_rejects_before_launch(lib):
 
 def test_quantize_validation_rejects_before_launch(lib):
     P = ctypes.c_void_p
-    assert lib.mla_quantize_fp8(P(1 << 20), 10, 0.0, P(1 << 24), None) == -1 and b"scale" in lib.mla_last_error()
-    assert lib.mla_quantize_fp8(P(1 << 20), -1, 1.0, P(1 << 24), None) == -1
-    assert lib.mla_quantize_fp8(P((1 << 20) + 8), 10, 1.0, P(1 << 24), None) == -1
-    assert lib.mla_quantize_fp8(None, 10, 1.0, P(1 << 24), None) == -1
-    assert lib.mla_quantize_fp8(None, 0, 1.0, None, None) == 0
+    x, o = P(1 << 20), P(1 << 24)
+    assert lib.mla_quantize_fp8(x, 64, 10, 64, 0.0, o, 64, None) == -1 and b"scale" in lib.mla_last_error()
+    assert lib.mla_quantize_fp8(x, 64, -1, 64, 1.0, o, 64, None) == -1
+    assert lib.mla_quantize_fp8(x, 64, 10, 60, 1.0, o, 64, None) == -1 and b"width" in lib.mla_last_error()
+    assert lib.mla_quantize_fp8(x, 32, 10, 64, 1.0, o, 64, None) == -1 and b"stride" in lib.mla_last_error()
+    assert lib.mla_quantize_fp8(P((1 << 20) + 8), 64, 10, 64, 1.0, o, 64, None) == -1
+    assert lib.mla_quantize_fp8(None, 64, 10, 64, 1.0, o, 64, None) == -1
+    assert lib.mla_quantize_fp8(None, 64, 0, 64, 1.0, None, 64, None) == 0
 
 
 def test_gather_validation_rejects_before_launch(lib):

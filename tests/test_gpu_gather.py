@@ -115,14 +115,29 @@ def test_gather_full_dsv3_contexts():
         del g
 
 
-@pytest.mark.parametrize("n", [1, 7, 8, 4096 * 128 + 5, 64 * 128 * 576])
-def test_quantize_fp8_bitexact(n):
+@pytest.mark.parametrize("rows,width", [(1, 8), (3, 64), (1000, 512), (64 * 128, 576)])
+def test_quantize_fp8_bitexact(rows, width):
     """scaled_fp8_quant on the GPU equals the oracle's float32 divide + e4m3
-    encoding bit for bit (values past the range saturate); ragged lengths."""
-    x = synth.bf16_normal(80 + n % 97, (n,), std=2.0)
+    encoding bit for bit (values past the range saturate)."""
+    x = synth.bf16_normal(80 + rows % 97, (rows, width), std=2.0)
     scale = float(np.float32(3.0 / 448.0))
     dev = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
-    out = torch.full((n,), 0x55, dtype=torch.uint8, device="cuda")
+    out = torch.full((rows, width), 0x55, dtype=torch.uint8, device="cuda")
     mla.quantize_fp8(dev, scale, out)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy(), oracle.quantize_fp8(x, scale))
+
+
+def test_quantize_fp8_into_query_rows():
+    """q_abs and q_pe quantised straight into the two column ranges of
+    [q_abs | q_pe] rows (strided output), the rest of each row untouched."""
+    T, N = 7, 16
+    qa = synth.bf16_normal(90, (T, N, 512))
+    qp = synth.bf16_normal(91, (T, N, 64))
+    scale = float(np.float32(2.5 / 448.0))
+    q8 = torch.full((T, N, 576), 0x55, dtype=torch.uint8, device="cuda")
+    mla.quantize_fp8(torch.from_numpy(qa.view(np.int16)).cuda().view(torch.bfloat16), scale, q8[..., :512])
+    mla.quantize_fp8(torch.from_numpy(qp.view(np.int16)).cuda().view(torch.bfloat16), scale, q8[..., 512:])
+    torch.cuda.synchronize()
+    want = np.concatenate([oracle.quantize_fp8(qa, scale), oracle.quantize_fp8(qp, scale)], axis=-1)
+    assert np.array_equal(q8.cpu().numpy(), want)
