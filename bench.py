@@ -357,7 +357,7 @@ def run_gpu(args):
     achieved_tf = alg["flops"] / (kms * 1e-3) / 1e12
     # the binding roof of the workload: bytes at the HBM peak or FLOPs at the tensor peak
     hbm_bound = alg["decode_bytes"] / (hbm * 1e9) >= alg["flops"] / (tflops * 1e12)
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(args.workload, [f"decode_{args.workload}_fp8q.md"] if fp8q else None)
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4)}

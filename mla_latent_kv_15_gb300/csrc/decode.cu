@@ -28,7 +28,13 @@
 //    ([8 chunks][rows][16 B]), so the 32 lanes of a warp write 512 contiguous
 //    bytes of the peer's shared memory per st.async instruction.
 //  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
-//    bf16 P (A operand of P.V) [464,496).
+//    bf16 P (A operand of P.V) [464,496).  With an e4m3 query the Q slice
+//    holds codes, four per column, and fills only [256,328).
+//  * e4m3 query over an e4m3 cache: the score MMAs are fp8 x fp8
+//    (kind::f8f6f4, K = 32) straight on the landed e4m3 boxes; only the
+//    value dims are widened to bf16 for P.V, after the tile's score MMAs
+//    are done with the codes; the partial scores are multiplied by
+//    q_scale * kv_scale before the exchange.
 //  * Warp roles: a TMA producer, a score-MMA issuer (+TMEM owner), a P.V-MMA
 //    issuer, four softmax / exchange / O rescale / epilogue warps (one query
 //    row per thread, the row's TMEM lane) and, for an e4m3 cache, four warps
@@ -140,7 +146,8 @@ constexpr size_t smem_bytes() {
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
                   smem_bytes<3>() <= 232448,
               "shared memory per CTA");
-static_assert(Layout<0>::kStages <= kMaxStages && Layout<1>::kStages <= kMaxStages && Layout<2>::kStages <= kMaxStages,
+static_assert(Layout<0>::kStages <= kMaxStages && Layout<1>::kStages <= kMaxStages &&
+                  Layout<2>::kStages <= kMaxStages && Layout<3>::kStages <= kMaxStages,
               "barrier arrays");
 
 struct Ctx {
