@@ -220,19 +220,25 @@ def quantize_fp8(x, scale: float, out, stream=None) -> None:
 
 
 def _row_pitch(t) -> int:
-    """Element distance between consecutive rows (last dimension = a row) of
-    a tensor whose rows are equally spaced with a contiguous last dimension."""
-    if t.dim() == 1:
-        return t.numel()
-    if t.stride(-1) != 1:
+    """Element distance between consecutive rows (the last dimension is a
+    row) of a tensor whose rows are equally spaced in memory with a contiguous
+    last dimension; dimensions of size 1 may carry any stride.  A tensor of
+    one row reports its width."""
+    if t.dim() == 0:
+        raise ValueError("a tensor of rows needs at least one dimension")
+    width = t.shape[-1]
+    if width > 1 and t.stride(-1) != 1:
         raise ValueError("the last dimension must be contiguous")
-    pitch = t.stride(-2)
-    expect = pitch
+    pitch, inner = None, 1          # inner: rows spanned by the dimensions inside d
     for d in range(t.dim() - 2, -1, -1):
-        if t.shape[d] > 1 and t.stride(d) != expect:
-            raise ValueError("rows must be equally spaced")
-        expect *= t.shape[d]
-    return pitch
+        n = t.shape[d]
+        if n > 1:
+            if pitch is None:
+                pitch = t.stride(d)
+            elif t.stride(d) != pitch * inner:
+                raise ValueError("rows must be equally spaced")
+        inner *= n
+    return width if pitch is None else pitch
 
 
 def proj_status(clear: bool = False, stream=None) -> int:

@@ -145,3 +145,24 @@ def test_product_fails_loudly_without_library(tmp_path):
             mla.load(str(tmp_path / "missing.so"))
     finally:
         mla._lib = saved
+
+
+def test_row_pitch_of_strided_tensors():
+    """The binding's row pitch (host logic of mla_quantize_fp8's wrapper):
+    column slices of wider rows, size-1 dimensions with any stride, and the
+    layouts it must refuse."""
+    import torch
+    from mla_latent_kv_15_gb300 import _row_pitch
+    q8 = torch.empty((7, 16, 576), dtype=torch.uint8)
+    assert _row_pitch(q8) == 576
+    assert _row_pitch(q8[..., :512]) == 576 and _row_pitch(q8[..., 512:]) == 576
+    assert _row_pitch(q8[3]) == 576 and _row_pitch(q8[3, 5]) == 576        # one row: its width
+    assert _row_pitch(torch.empty((5, 1, 64)).transpose(0, 1)) == 64      # size-1 dim, any stride
+    assert _row_pitch(torch.empty((1, 1, 64))) == 64
+    assert _row_pitch(q8[:, :1, :512]) == 16 * 576                        # one head of each token
+    with pytest.raises(ValueError):
+        _row_pitch(q8[::2])                                                # gaps between tokens
+    with pytest.raises(ValueError):
+        _row_pitch(q8.transpose(1, 2))                                     # non-contiguous rows
+    with pytest.raises(ValueError):
+        _row_pitch(torch.empty(()))
