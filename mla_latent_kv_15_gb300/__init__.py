@@ -90,7 +90,14 @@ def _check(rc: int) -> None:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a CUDA tensor (None passes NULL).  Every tensor the
+    library reads or writes lives on the GPU: a host tensor is refused here,
+    before its address could reach a kernel."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -112,7 +119,8 @@ def _dtype_code(cache):
 def cache_write(kv_c, k_pe, slot_mapping, cache, kv_scale: float = 1.0, stream=None) -> None:
     """concat_and_cache_mla: cache[num_blocks, page, 576] (bf16 or float8_e4m3fn)."""
     nb, ps, w = cache.shape
-    assert w == DQK
+    if w != DQK:
+        raise ValueError(f"cache rows must be {DQK} wide, got {w}")
     _check(load().mla_cache_write(_ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), slot_mapping.numel(), _ptr(cache),
                                   nb, ps, _dtype_code(cache), float(kv_scale), _stream(stream)))
 
@@ -199,7 +207,8 @@ def gather_cache(cache, block_table, cu_seq_lens, dst, seq_starts=None, kv_scale
     """gather_and_maybe_dequant_cache: dst [num_tokens, 576] bf16 receives the
     chunk rows of every request (cu_seq_lens [B+1], seq_starts [B] int32)."""
     nb, ps, w = cache.shape
-    assert w == DQK
+    if w != DQK:
+        raise ValueError(f"cache rows must be {DQK} wide, got {w}")
     B = cu_seq_lens.numel() - 1
     _check(load().mla_gather_cache(_ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale), _ptr(block_table),
                                    block_table.shape[1], _ptr(cu_seq_lens), _ptr(seq_starts), B, _ptr(dst),

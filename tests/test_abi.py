@@ -166,3 +166,17 @@ def test_row_pitch_of_strided_tensors():
         _row_pitch(q8.transpose(1, 2))                                     # non-contiguous rows
     with pytest.raises(ValueError):
         _row_pitch(torch.empty(()))
+
+
+def test_binding_refuses_host_tensors_and_bad_cache_width():
+    """The binding hands the library device addresses only: host tensors and
+    caches of the wrong row width are refused before any call."""
+    import torch
+    import mla_latent_kv_15_gb300 as mla
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mla._ptr(torch.empty(4))
+    assert mla._ptr(None) is None
+    with pytest.raises(ValueError, match="576"):
+        mla.cache_write(None, None, None, torch.empty((2, 64, 512), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="576"):
+        mla.gather_cache(torch.empty((2, 64, 512), dtype=torch.bfloat16), None, torch.zeros(2), None)
