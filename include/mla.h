@@ -285,7 +285,7 @@ MLA_API int mla_proj_status(int* status, int clear, void* stream);
  * float32 accumulation); P.V stays bf16 x bf16 (values expanded exactly).
  *   q_fp8     [total_q, num_heads, 576] e4m3 codes, rows [q_abs | q_pe]
  *             quantised with q_scale (mla_quantize_fp8), 16-byte aligned
- *   q_scale   finite and > 0
+ *   q_scale   finite and > 0, with q_scale * kv_scale a normal float32
  *   the cache must be e4m3 (kv_scale finite and > 0); every other argument,
  *   the output, the LSE, the workspace and the error behaviour are those of
  *   mla_decode.

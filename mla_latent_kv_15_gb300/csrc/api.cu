@@ -121,6 +121,8 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
     return fail(MLA_ERR_UNSUPPORTED, "an e4m3 query needs an e4m3 cache");
   if (q8 && !(std::isfinite(q_scale) && q_scale > 0.f))
     return fail(MLA_ERR_INVALID_ARG, "q_scale must be finite and > 0");
+  if (q8 && !(std::isnormal(q_scale * kv_scale)))
+    return fail(MLA_ERR_INVALID_ARG, "q_scale * kv_scale must be a normal float (the scores' code-product factor)");
   if (!aligned(block_table, 4) || !aligned(seq_lens, 4) || (query_start_loc && !aligned(query_start_loc, 4)) ||
       (lse && !aligned(lse, 4)))
     return fail(MLA_ERR_INVALID_ARG, "block_table, seq_lens, query_start_loc and lse must be 4-byte aligned");

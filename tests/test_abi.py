@@ -180,3 +180,23 @@ def test_binding_refuses_host_tensors_and_bad_cache_width():
         mla.cache_write(None, None, None, torch.empty((2, 64, 512), dtype=torch.bfloat16))
     with pytest.raises(ValueError, match="576"):
         mla.gather_cache(torch.empty((2, 64, 512), dtype=torch.bfloat16), None, torch.zeros(2), None)
+
+
+def test_fp8_query_decode_validation_rejects_before_launch(lib):
+    """mla_decode_fp8q refuses bad scales, a misaligned or missing query and a
+    short workspace on the host; an empty batch is a no-op."""
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def call(q=fake, q_scale=0.5, kv_scale=0.01, batch=2, total_q=2, ws_bytes=1 << 30):
+        return lib.mla_decode_fp8q(q, q_scale, fake, 10, 64, kv_scale, fake, 4, fake, batch, None, total_q, 16,
+                                   0.1, 0, fake, None, fake, ws_bytes, None)
+
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(q_scale=bad) == -1 and b"q_scale" in lib.mla_last_error()
+    assert call(kv_scale=0.0) == -1
+    assert call(q_scale=1e-30, kv_scale=1e-30) == -1 and b"normal" in lib.mla_last_error()
+    assert call(q=P((1 << 20) + 8)) == -1 and b"aligned" in lib.mla_last_error()
+    assert call(q=None) == -1 and b"null" in lib.mla_last_error()
+    assert call(ws_bytes=16) != 0 and b"workspace" in lib.mla_last_error()
+    assert call(batch=0, total_q=0) == 0
