@@ -400,7 +400,8 @@ def run_gpu(args):
                 "h2d_bytes_per_step": inp_bytes, "d2h_bytes_per_step": out_bytes,
                 "copies": "pinned host buffers; step i+1's inputs and step i's outputs move on copy streams "
                           "while step i computes (two device buffer sets)"},
-        "gpu_launches": 4 * args.steps,
+        # per step: cache write, plan, decode, combine (+ two query quantisations with an e4m3 query)
+        "gpu_launches": (6 if fp8q else 4) * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
