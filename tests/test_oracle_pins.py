@@ -172,6 +172,35 @@ def test_brute_force_tiny_against_scipy():
                 assert np.max(np.abs(out[r] - w @ rows[:L, :LKV])) <= 1e-12
 
 
+def test_brute_force_tiny_e4m3_cache_against_scipy():
+    """The e4m3 branch of the decode: keys and values are the stored codes'
+    OCP values times kv_scale.  Tiny contexts through a permuted table of
+    4-row pages, against numpy dots and scipy's logsumexp on rows decoded
+    independently of the decode (an unscaled value, a scale applied to the
+    keys only or twice, or a wrong gather fails)."""
+    case = synth.make_decode_case(num_heads=3, batch=4, ctx=(1, 9), sq=[1, 2, 1, 3], page_size=4,
+                                  num_blocks=16, seed=24, cache_dtype="fp8", poison=False)
+    cache = oracle.prepare_cache(case, with_new_rows=False)
+    out, lse, _ = oracle.decode_case(case, cache)
+    kvs = float(np.float32(case.kv_scale))
+    q = np.concatenate([oracle.bf16_to_f64(case.q_abs), oracle.bf16_to_f64(case.q_pe)], -1)
+    qsl = case.query_start_loc
+    for b in range(case.batch):
+        pos = np.arange(int(case.seq_lens[b]))
+        codes = cache[case.block_table[b, pos // case.page_size], pos % case.page_size]
+        rows = oracle.e4m3_to_f64(codes) * kvs
+        sq = qsl[b + 1] - qsl[b]
+        for tl in range(sq):
+            t = qsl[b] + tl
+            L = case.seq_lens[b] - sq + 1 + tl
+            for h in range(3):
+                s = case.scale * (rows[:L] @ q[t, h])
+                w = np.exp(s - logsumexp(s))
+                r = t * 3 + h
+                assert abs(lse[r] - logsumexp(s)) <= 1e-12
+                assert np.max(np.abs(out[r] - w @ rows[:L, :LKV])) <= 1e-12
+
+
 def test_causal_rule_closed_form():
     """q = 0 makes every visible score 0, so o is the mean of the visible rows
     and lse = ln L.  With kv_c[:, 0] = position, o[0] = (L - 1) / 2, where the
