@@ -55,3 +55,27 @@ def test_reference_arm_other_ranks_exit_quietly():
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_algorithmic_bytes_and_flops_by_hand():
+    """The roofline's numerator: every visible latent row read once, queries
+    read, outputs and LSE written; 2 * (576 + 512) FLOP per visible (key,
+    query row), with the multi-token causal window (token t of an Sq-token
+    request sees seq_len - Sq + 1 + t keys)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    N = 4
+    case = synth.make_decode_case(num_heads=N, batch=3, ctx=(1, 1), sq=[1, 1, 2], seq_lens=[5, 0, 3],
+                                  page_size=16, seed=3, poison=False)
+    a = bench.algorithmic(case)
+    T = 4
+    assert a["kv"] == (5 + 0 + 3) * 576 * 2
+    assert a["q"] == T * N * 576 * 2
+    assert a["out"] == T * N * (512 * 2 + 4)
+    assert a["decode_bytes"] == a["kv"] + a["q"] + a["out"]
+    visible = 5 + 0 + (2 + 3)
+    assert a["flops"] == 2 * (576 + 512) * N * visible
+    fp8 = synth.make_decode_case(num_heads=N, batch=3, ctx=(1, 1), sq=[1, 1, 2], seq_lens=[5, 0, 3],
+                                 page_size=16, seed=3, poison=False, cache_dtype="fp8")
+    assert bench.algorithmic(fp8)["kv"] == 8 * 576
