@@ -63,8 +63,8 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-def _normal_bf16_pages(seed: int, npages: int, page_size: int) -> np.ndarray:
-    """N(0,1)*0.5 latent rows for `npages` pages as bf16 bits, drawn in chunks of
+def _normal_bf16_pages(seed: int, npages: int, page_size: int, std: float = 0.5) -> np.ndarray:
+    """N(0,1)*std latent rows for `npages` pages as bf16 bits, drawn in chunks of
     256 pages, each from its own PCG64 stream spawned from `seed` (the result
     does not depend on how many threads draw them)."""
     import concurrent.futures as cf
@@ -77,7 +77,7 @@ def _normal_bf16_pages(seed: int, npages: int, page_size: int) -> np.ndarray:
         lo, hi = i * chunk, min(npages, (i + 1) * chunk)
         g = np.random.Generator(np.random.PCG64(seqs[i]))
         v = g.standard_normal((hi - lo, page_size, DQK), dtype=np.float32)
-        v *= np.float32(0.5)
+        v *= np.float32(std)
         out[lo:hi] = to_bf16_bits(v)
 
     with cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 4)) as ex:
@@ -128,13 +128,21 @@ def make_decode_case(*, num_heads: int, batch: int, ctx: tuple[int, int], sq=1,
                      page_size: int = 64, num_blocks: int | None = None,
                      cache_dtype: str = "bf16", seed: int = 0, poison: bool = True,
                      seq_lens=None, qk_nope_dim: int = 128, qk_rope_dim: int = ROPE,
-                     max_pages: int | None = None, name: str = "") -> DecodeCase:
+                     max_pages: int | None = None, name: str = "", q_std: float = 0.5,
+                     kv_std: float = 0.5, rising: float = 0.0, rising_q: float = 4.0) -> DecodeCase:
     """Draw one decode batch.
 
     ``sq`` is an int (same number of query tokens for every request) or a list
     of per-request counts.  ``seq_lens`` may be given explicitly (edge cases);
     otherwise lengths are uniform in ``ctx``.  With ``poison`` the pages no
     request references hold bf16 NaN, so a wrong gather cannot go unnoticed.
+
+    Sharper attention: ``q_std`` and ``kv_std`` are the standard deviations of
+    the query and latent-row draws (0.5 by default).  ``rising`` > 0 writes
+    ``rising * j`` into the first rope dimension of the row at context
+    position j of every request (the step's new rows included) and sets the
+    first rope dimension of every query to ``rising_q``, so that scores grow
+    along the context and the running maximum of a row keeps rising.
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     sqs = np.asarray([sq] * batch if np.isscalar(sq) else list(sq), dtype=np.int64)
@@ -160,7 +168,9 @@ def make_decode_case(*, num_heads: int, batch: int, ctx: tuple[int, int], sq=1,
     qsl[1:] = np.cumsum(sqs)
     total_q = int(qsl[-1])
 
-    q = rng.standard_normal((total_q, num_heads, DQK), dtype=np.float32) * np.float32(0.5)
+    q = rng.standard_normal((total_q, num_heads, DQK), dtype=np.float32) * np.float32(q_std)
+    if rising > 0:
+        q[:, :, LKV] = np.float32(rising_q)
     qb = to_bf16_bits(q)
     pool = np.empty((num_blocks, page_size, DQK), dtype=np.uint16)
     used = table[table >= 0]
@@ -169,8 +179,17 @@ def make_decode_case(*, num_heads: int, batch: int, ctx: tuple[int, int], sq=1,
     else:
         pool[...] = 0
     if used.size:
-        pool[used] = _normal_bf16_pages(seed, used.size, page_size)
-    new = rng.standard_normal((total_q, DQK), dtype=np.float32) * np.float32(0.5)
+        pool[used] = _normal_bf16_pages(seed, used.size, page_size, kv_std)
+    new = rng.standard_normal((total_q, DQK), dtype=np.float32) * np.float32(kv_std)
+    if rising > 0:
+        # position of each new row: the last Sq positions of its request
+        pos_new = np.concatenate([np.arange(int(lens[b]) - int(sqs[b]), int(lens[b])) for b in range(batch)]) \
+            if total_q else np.zeros(0, dtype=np.int64)
+        new[:, LKV] = np.float32(rising) * np.maximum(pos_new, 0).astype(np.float32)
+        for b in range(batch):
+            for lp in range(int(pages[b])):
+                pos = lp * page_size + np.arange(page_size)
+                pool[table[b, lp], :, LKV] = to_bf16_bits(np.float32(rising) * pos.astype(np.float32))
     newb = to_bf16_bits(new)
 
     # slots of the new tokens: the last Sq positions of each sequence
