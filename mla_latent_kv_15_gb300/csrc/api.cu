@@ -16,6 +16,9 @@ namespace {
 
 thread_local std::string g_last_error;
 thread_local cudaEvent_t g_timing_start = nullptr, g_timing_stop = nullptr;
+// bounded-wait test settings of the calling thread (mla_set_decode_wait_test)
+thread_local int g_test_skip_tile = 0;
+thread_local unsigned long long g_wait_limit_ns = 1000000000ull;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -62,6 +65,15 @@ const char* mla_last_error(void) { return g_last_error.c_str(); }
 int mla_set_decode_timing_events(void* start, void* stop) {
   g_timing_start = start && stop ? static_cast<cudaEvent_t>(start) : nullptr;
   g_timing_stop = start && stop ? static_cast<cudaEvent_t>(stop) : nullptr;
+  return ok();
+}
+
+int mla_set_decode_wait_test(int skip_first_tile, unsigned long long wait_limit_ns) {
+  if (wait_limit_ns == 0) wait_limit_ns = 1000000000ull;
+  if (wait_limit_ns < 100000ull || wait_limit_ns > 1000000000ull)
+    return fail(MLA_ERR_INVALID_ARG, "wait_limit_ns must be 0 (default 1 s) or in [1e5, 1e9]");
+  g_test_skip_tile = skip_first_tile != 0;
+  g_wait_limit_ns = wait_limit_ns;
   return ok();
 }
 
@@ -149,29 +161,44 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   const int clusters = sms / 2 < mla::kMaxClusters ? sms / 2 : mla::kMaxClusters;
 
   const uint64_t rows = (uint64_t)total_q * num_heads;
-  CUtensorMap tm_q, tm_qpe, tm_kv;
+  const uint64_t kv_rows = (uint64_t)num_blocks * page_size;
+  // Each CTA of a pair reads latent columns [256r, 256r+256) and rope columns
+  // [512+32r, 512+32r+32): tensor maps for the latent boxes and the rope boxes
+  // of the query and of the cache.
+  CUtensorMap tm_q, tm_qr, tm_kv, tm_kvr;
   const uint32_t kv_box_rows = page_size < mla::kTile ? page_size : mla::kTile;
+  bool enc;
   if (q8) {
-    // e4m3 query rows and cache rows (576 wide) in 128-dim, 128-byte-swizzled boxes
-    if (!mla::encode_tmap_2d(&tm_q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, rows, mla::kDqk, 128, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk,
-                             (uint64_t)num_blocks * page_size, mla::kDqk, 128, kv_box_rows,
-                             CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
-    tm_qpe = tm_q;   // not read by the e4m3-query kernel
-  } else if (!mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64,
-                                  64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !mla::encode_tmap_2d(&tm_qpe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 64, 64,
-                           CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !(cache_dtype == MLA_BF16
-            ? mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk,
-                                  (uint64_t)num_blocks * page_size, mla::kDqk * 2, 64, kv_box_rows,
-                                  CU_TENSOR_MAP_SWIZZLE_128B)
-            : mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk,
-                                  (uint64_t)num_blocks * page_size, mla::kDqk, 64, kv_box_rows,
-                                  CU_TENSOR_MAP_SWIZZLE_NONE)))
-    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
+    // e4m3 query rows and cache rows (576 bytes wide): 128-byte latent boxes
+    // (128-B swizzle) and 32-byte rope boxes (32-B swizzle)
+    enc = mla::encode_tmap_2d(&tm_q, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, rows, mla::kDqk, 128, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B) &&
+          mla::encode_tmap_2d(&tm_qr, q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, rows, mla::kDqk, 32, 64,
+                              CU_TENSOR_MAP_SWIZZLE_32B) &&
+          mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, kv_rows, mla::kDqk, 128,
+                              kv_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+          mla::encode_tmap_2d(&tm_kvr, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, kv_rows, mla::kDqk, 32,
+                              kv_box_rows, CU_TENSOR_MAP_SWIZZLE_32B);
+  } else {
+    // bf16 q_abs (64-dim boxes, 128-B swizzle) and q_pe (32-dim boxes, 64-B swizzle)
+    enc = mla::encode_tmap_2d(&tm_q, q_abs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64, 64,
+                              CU_TENSOR_MAP_SWIZZLE_128B) &&
+          mla::encode_tmap_2d(&tm_qr, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kRope, rows, mla::kRope * 2, 32,
+                              64, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (cache_dtype == MLA_BF16)
+      enc = enc &&
+            mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk, kv_rows, mla::kDqk * 2,
+                                64, kv_box_rows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            mla::encode_tmap_2d(&tm_kvr, cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kDqk, kv_rows, mla::kDqk * 2,
+                                32, kv_box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
+    else  // e4m3 codes land unswizzled and are expanded on chip
+      enc = enc &&
+            mla::encode_tmap_2d(&tm_kv, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, kv_rows, mla::kDqk, 64,
+                                kv_box_rows, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            mla::encode_tmap_2d(&tm_kvr, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, kv_rows, mla::kDqk, 32,
+                                kv_box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!enc) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
 
   mla::DecodeArgs a{};
   a.block_table = block_table;
@@ -197,6 +224,8 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   a.out_scale = kvs;
   a.out = out;
   a.lse = lse;
+  a.wait_limit_ns = g_wait_limit_ns;
+  a.debug_skip_tile = g_test_skip_tile;
   a.plan = mla::plan_from_workspace(workspace, L);
 
   cudaStream_t s = (cudaStream_t)stream;
@@ -211,7 +240,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
-  e = mla::launch_decode(tm_q, tm_qpe, tm_kv, variant, a, clusters, s);
+  e = mla::launch_decode(tm_q, tm_qr, tm_kv, tm_kvr, variant, a, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
   e = mla::launch_combine(a, L.max_groups, s);

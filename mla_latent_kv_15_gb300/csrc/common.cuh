@@ -118,6 +118,8 @@ struct DecodeArgs {
   float qk_scale;           // e4m3 query: q_scale * kv_scale (code products -> scores)
   void* out;                // bf16 [T*N, 512]
   float* lse;               // [T*N] or null
+  unsigned long long wait_limit_ns;   // bound of every on-chip wait (1 s)
+  int debug_skip_tile;      // test aid: CTA 0 of cluster 0 never loads its first cache tile
   Plan plan;
 };
 
@@ -126,9 +128,14 @@ struct DecodeArgs {
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s);
 // variant: 0 bf16 cache, 1 e4m3 cache, 2 bf16 cache with <= 32-row groups
-// (plan built with group_rows = 32), 3 e4m3 query and e4m3 cache
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv, int variant,
-                          const DecodeArgs& a, int num_clusters, cudaStream_t s);
+// (plan built with group_rows = 32), 3 e4m3 query and e4m3 cache.  Tensor
+// maps: the query's latent columns (64-dim boxes; 128-dim e4m3 boxes for
+// variant 3) and its rope columns (32-dim boxes), the cache's latent columns
+// and its rope columns, boxes as wide (rows: min(page, 64) for the cache, 64
+// for the query).
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
+                          const CUtensorMap& tm_kvr, int variant, const DecodeArgs& a, int num_clusters,
+                          cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                                 int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,

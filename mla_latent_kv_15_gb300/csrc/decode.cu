@@ -11,22 +11,30 @@
 // Design (one work unit = <=128 query rows of one request x a tile range):
 //  * The query rows of a unit form the M = 128 dimension of every MMA.
 //  * A cluster of two CTAs shares each 64-key tile.  CTA r owns
-//      - half of the score contraction, dims [288r, 288r+288): it loads only
-//        those columns of the cached rows (plus the 64-dim box they straddle)
-//        and keeps its 288 query dims in TMEM as the A operand;
-//      - half of the output, dims [256r, 256r+256) of O += P . V.
+//      - dims [256r, 256r+256) of the latent output, O += P . V;
+//      - half of the score contraction: the same 256 latent dims plus rope
+//        dims [32r, 32r+32), i.e. cache columns [256r, 256r+256) and
+//        [512+32r, 512+32r+32).  It loads exactly those columns of every
+//        cached row (the pair reads each cached byte once) and keeps the
+//        matching 288 query dims in TMEM as the A operand.
 //    Each CTA computes a partial score tile S_r (18 MMAs, N = 64 keys), stores
-//    it into the peer's shared memory as fp16 (st.async over the cluster
-//    network), and adds the peer's partial to its own (fp32) partial.  Nothing
-//    is computed twice and every cached byte is read from HBM once.
+//    it into the peer's shared memory (st.async over the cluster network), and
+//    adds the peer's partial to its own.  Nothing is computed twice.
+//  * Exchange format: 16-bit block fixed point.  Per row and tile the sender
+//    takes the range [lo, hi] of its partials over the keys the row may see
+//    and sends 16-bit codes of (s - c) / step, c = (lo + hi) / 2, step = half
+//    range / 32766, with c and step as an 8-byte row header.  The absolute
+//    error is at most step / 2 whatever the magnitude of the partials (fp16
+//    would lose 2^-11 of |s|, a problem once partials reach hundreds).  The
+//    receiver folds c into the row's maximum and the exponent's offset.
 //  * The exchange of tile i+1 is issued before tile i is processed, so the
 //    network transfer overlaps the softmax of the previous tile.  Partials
 //    land in a ring of four receive buffers that needs no return handshake:
 //    a CTA writes tile i+1 into the buffer of tile i-3 only after it has
 //    received tile i-1 from the peer, and the peer sent tile i-1 only after
-//    all its softmax threads had read tile i-3.  The buffers are chunk-major
-//    ([8 chunks][rows][16 B]), so the 32 lanes of a warp write 512 contiguous
-//    bytes of the peer's shared memory per st.async instruction.
+//    all its softmax threads had read tile i-3.  The code part of a buffer is
+//    chunk-major ([8 chunks][rows][16 B]), so the 32 lanes of a warp write
+//    512 contiguous bytes of the peer's shared memory per st.async.
 //  * TMEM (512 columns): O half [0,256), Q slice [256,400), S [400,464),
 //    bf16 P (A operand of P.V) [464,496).  With an e4m3 query the Q slice
 //    holds codes, four per column, and fills only [256,328).
@@ -46,9 +54,12 @@
 //    any reference m.  CTA 0 writes the LSE.
 //  * Split units write fp32 partials (normalised o and lse) that the combine
 //    kernel merges (merge_attn_states rule).
-//  * Every mbarrier wait is bounded (1 s); on expiry the CTA raises its abort
-//    flag and the error word, skips all further waits and runs to the end
-//    without touching memory outside its buffers.
+//  * Every mbarrier wait is bounded (1 s unless the launch asks for less); on
+//    expiry the CTA raises its abort flag and the error word, skips its local
+//    waits and runs to the end without touching memory outside its buffers.
+//    Waits for the peer's partial scores stay bounded waits even then (at most
+//    1 ms each once aborted), so no store of the peer is still in flight into
+//    this CTA's shared memory when it exits.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -62,33 +73,43 @@ namespace {
 using namespace ptx;
 
 constexpr int kBox = 64 * 128;                    // 64 rows x 64 bf16 (128 B rows, 128-B swizzle)
-constexpr int kBoxesPerStage = 5;                 // each CTA loads 5 of the 9 column boxes
-constexpr int kStageBytes = kBoxesPerStage * kBox;
-constexpr int kFp8Box = 64 * 64;                  // 64 rows x 64 e4m3 (64 B rows, no swizzle)
-constexpr int kFp8TileBytes = kBoxesPerStage * kFp8Box;
-// An e4m3 tile lands in the upper half of the bf16 stage it is expanded into.
+constexpr int kVBoxes = 4;                        // the CTA's 256 latent dims: values and scores
+constexpr int kRopeBox = 64 * 64;                 // 64 rows x 32 bf16 rope dims (64 B rows, 64-B swizzle)
+constexpr int kRopeOff = kVBoxes * kBox;          // rope half-box after the four latent boxes
+constexpr int kStageBytes = kRopeOff + kRopeBox;  // 36 KB: every cached column the CTA reads
+static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of the 128-B swizzle");
+// e4m3 cache, bf16 query (variant 1): the CTA's e4m3 tile lands unswizzled in
+// the top of its bf16 slot (four 64 x 64-byte boxes, then the 64 x 32-byte
+// rope half-box) and is expanded in place into the bf16 layout above.
+constexpr int kFp8Box = 64 * 64;
+constexpr int kFp8RopeBox = 64 * 32;
+constexpr int kFp8TileBytes = kVBoxes * kFp8Box + kFp8RopeBox;   // 18 KB
 constexpr int kFp8InPlace = kStageBytes - kFp8TileBytes;
-// e4m3 query and cache (variant 3): each item lands as three 128-dim boxes
-// (64 rows x 128 e4m3, 128-B swizzle) that the fp8 score MMAs read directly,
-// in the top 24 KB of the slot; the value dims are then expanded to bf16
-// below them (boxes 0-3 of the slot), once the score MMAs are done.
+// e4m3 query and cache (variant 3): each item lands as two 128-dim boxes (64
+// rows x 128 e4m3, 128-B swizzle) and one 32-dim rope box (64 rows x 32 e4m3,
+// 32-B swizzle) that the fp8 score MMAs read directly, in the top 18 KB of
+// the slot; the value dims (the two 128-dim boxes) are then expanded to bf16
+// into boxes 0-3 of the slot, once the tile's score MMAs are done.
 constexpr int kQ8Box = 64 * 128;
-constexpr int kQ8Boxes = 3;
-constexpr int kQ8Bytes = kQ8Boxes * kQ8Box;
+constexpr int kQ8RopeBox = 64 * 32;
+constexpr int kQ8Bytes = 2 * kQ8Box + kQ8RopeBox;
 constexpr int kQ8InPlace = kStageBytes - kQ8Bytes;
 static_assert(kQ8InPlace % 1024 == 0 && kQ8InPlace + kQ8Bytes == kStageBytes, "e4m3 landing area");
 // Kernel variants: 0 bf16 cache; 1 e4m3 cache (expanded in place in the bf16
 // ring); 3 e4m3 query and e4m3 cache (fp8 score MMAs, values expanded for
-// P.V); 2 bf16 cache with at most 32
-// query rows per unit (small head counts: the receive ring shrinks to 32-row
-// buffers and the cache ring gets a fifth stage).
+// P.V); 2 bf16 cache with at most 32 query rows per unit (small head counts:
+// the receive ring shrinks to 32-row buffers and the cache ring gets a fifth
+// stage).
 template <int kVariant>
 struct Layout {
   static constexpr int kStages = kVariant == 2 ? 5 : 4;
   static constexpr int kXRows = kVariant == 2 ? 32 : kRows;        // rows of a receive buffer
-  static constexpr int kXBytes = kXRows * kTile * 2;              // one fp16 partial score tile
+  static constexpr int kXChunk = kXRows * 16;                      // one 16-byte chunk of every row
+  static constexpr int kXHdr = 8 * kXChunk;                        // row headers after the 8 code chunks
+  static constexpr int kXBytes = kXHdr + kXRows * 8;               // codes + (centre, step) per row
 };
 constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
+constexpr uint32_t kXRowBytes = kTile * 2 + 8;    // exchanged bytes per row and tile
 // Warp roles.
 //  bf16 cache (224 threads): 0 TMA producer, 1 score-MMA issuer (and TMEM
 //    owner), 2 P.V-MMA issuer, 3-6 softmax.
@@ -115,6 +136,11 @@ constexpr uint32_t kTmemQ = 256;
 constexpr uint32_t kTmemS = kTmemQ + kQCols;      // 400
 constexpr uint32_t kTmemP = kTmemS + kTile;       // 464
 constexpr float kRescaleThreshold = 8.0f;         // log2 units
+// Exchange codes: c + (u - 32768) * step, u in [1, 65535].  A float of value
+// 12582912 + u (1.5 * 2^23 + u) holds u in its low 16 bits.
+constexpr float kCodeMagic = 12582912.0f + 32768.0f;
+constexpr float kCodeRange = 32766.0f;            // |code| <= 32766 leaves a margin for rounding
+constexpr uint64_t kAbortWaitNs = 1000000ull;     // bound of a peer wait once the CTA has aborted
 
 static_assert(kTmemP + kTile / 2 <= 512, "TMEM columns");
 
@@ -123,7 +149,7 @@ constexpr int kMaxStages = 5;
 struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
   uint64_t kv_empty[kMaxStages];  // 2 arrivals: score issuer + P.V issuer (or 2 from the softmax for query items)
-  uint64_t stg_full[kMaxStages];  // e4m3 tile landed in the upper half of its ring slot
+  uint64_t stg_full[kMaxStages];  // e4m3 tile landed in the upper part of its ring slot
   uint64_t kx_free[kMaxStages];   // variant 3: the slot's score MMAs are done (its e4m3 boxes may be overwritten)
   uint64_t q_ready;
   uint64_t s_full;
@@ -149,10 +175,12 @@ static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_byt
 static_assert(Layout<0>::kStages <= kMaxStages && Layout<1>::kStages <= kMaxStages &&
                   Layout<2>::kStages <= kMaxStages && Layout<3>::kStages <= kMaxStages,
               "barrier arrays");
+static_assert(Layout<0>::kXBytes % 16 == 0 && Layout<2>::kXBytes % 16 == 0, "receive buffers 16-byte aligned");
 
 struct Ctx {
   Barriers* bars;
   int* status;
+  uint64_t limit_ns;
 };
 
 __device__ __forceinline__ void raise_error(const Ctx& c, int bit) {
@@ -160,14 +188,19 @@ __device__ __forceinline__ void raise_error(const Ctx& c, int bit) {
   atomicOr(c.status, bit);
 }
 
-// Bounded waits; once the CTA has aborted every wait returns at once.
+// Bounded waits on this CTA's own pipeline; once the CTA has aborted they
+// return at once.
 __device__ __forceinline__ void wait_bar(const Ctx& c, uint64_t* bar, uint32_t parity) {
   if (*(volatile int*)&c.bars->abort) return;
-  if (!mbar_wait(smem_u32(bar), parity)) raise_error(c, 1);
+  if (!mbar_wait(smem_u32(bar), parity, c.limit_ns)) raise_error(c, 1);
 }
+// Bounded wait for the peer's partial scores.  It is kept after an abort
+// (with a 1 ms bound): the peer's stores into this CTA's receive buffers must
+// land before the CTA exits.
 __device__ __forceinline__ void wait_bar_cluster(const Ctx& c, uint64_t* bar, uint32_t parity) {
-  if (*(volatile int*)&c.bars->abort) return;
-  if (!mbar_wait_cluster(smem_u32(bar), parity)) raise_error(c, 1);
+  const bool aborted = *(volatile int*)&c.bars->abort;
+  const uint64_t lim = aborted && c.limit_ns > kAbortWaitNs ? kAbortWaitNs : c.limit_ns;
+  if (!mbar_wait_cluster(smem_u32(bar), parity, lim)) raise_error(c, 1);
 }
 
 __device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -217,69 +250,123 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
+// acc = d * b + acc for a pair (vector addend)
+__device__ __forceinline__ void fma2v(float& acc0, float& acc1, float d0, float d1, float b) {
+  asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %4};\n mov.b64 z, {%0, %1};\n"
+      " fma.rn.f32x2 z, x, y, z;\n mov.b64 {%0, %1}, z;\n}" : "+f"(acc0), "+f"(acc1) : "f"(d0), "f"(d1), "f"(b));
 }
 
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+// three-input min
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
-// Score-contraction K steps of CTA `rank`: 18 steps of 16 dims over its 288
-// dims, as (box position in the stage, 16-dim step inside the box).
-// rank 0: boxes 0-3 (all 4 steps) + box 4 steps 0,1 (dims 256-287)
-// rank 1: box 0 steps 2,3 (dims 288-319) + boxes 1-4 (all 4 steps)
-__device__ __forceinline__ bool kstep_valid(uint32_t rank, int p, int k) {
-  return rank == 0 ? (p < 4 || k < 2) : (p > 0 || k >= 2);
-}
-// Variant 3: 32-dim K steps of the three 128-dim e4m3 boxes.  CTA 0 (dims
-// 0-383 loaded) uses dims 0-287; CTA 1 (dims 256-639 loaded) uses 288-575.
-__device__ __forceinline__ constexpr bool kstep8_valid(uint32_t rank, int p, int k) {
-  return rank == 0 ? (p < 2 || k == 0) : (p == 1 || (p == 0 && k >= 1) || (p == 2 && k < 2));
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
 }
 
-// Expand one e4m3 tile (5 boxes x 64 rows x 64 B, row-major, in the upper
-// half of the ring slot) into the bf16 128-byte-swizzled layout the MMAs read
-// (what a bf16 TMA load would have written), in place: every thread first
+// Maximum and minimum of 64 values (NaN entries are ignored: max/min return
+// the other operand).
+__device__ __forceinline__ float max64(const float (&x)[kTile]) {
+  float m[22];
+#pragma unroll
+  for (int c = 0; c < 21; ++c) m[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
+  m[21] = x[63];
+#pragma unroll
+  for (int c = 0; c < 7; ++c) m[c] = fmax3(m[3 * c], m[3 * c + 1], m[3 * c + 2]);
+  m[7] = m[21];
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
+}
+__device__ __forceinline__ float min64(const float (&x)[kTile]) {
+  float m[22];
+#pragma unroll
+  for (int c = 0; c < 21; ++c) m[c] = fmin3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
+  m[21] = x[63];
+#pragma unroll
+  for (int c = 0; c < 7; ++c) m[c] = fmin3(m[3 * c], m[3 * c + 1], m[3 * c + 2]);
+  m[7] = m[21];
+  return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
+}
+
+// Maximum and minimum over the first n of 64 values (n >= 64: all), the
+// others left out; both NaN if n <= 0.
+__device__ __forceinline__ void range64(const float (&x)[kTile], int n, float& hi, float& lo) {
+  if (n >= kTile) {
+    hi = max64(x);
+    lo = min64(x);
+    return;
+  }
+  const float nan = __int_as_float(0x7fffffff);
+  float y[kTile];
+#pragma unroll
+  for (int c = 0; c < kTile; ++c) y[c] = c < n ? x[c] : nan;
+  hi = max64(y);
+  lo = min64(y);
+}
+
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] & 0xFFFF), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] >> 16), __NV_E4M3);
+    const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+    const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    o[2 * j] = pack_bf16x2(flo.x, flo.y);
+    o[2 * j + 1] = pack_bf16x2(fhi.x, fhi.y);
+  }
+}
+
+// Expand one e4m3 tile (four 64 x 64-byte latent boxes and one 64 x 32-byte
+// rope box, row-major, at the top of the ring slot) into the bf16 layouts the
+// MMAs read (what bf16 TMA loads would have written: 128-byte-swizzled
+// latent boxes, a 64-byte-swizzled rope box), in place: every thread first
 // reads its share of the whole tile, then all write.  e4m3 -> f16 -> f32 ->
 // bf16 is exact: every e4m3 value is a bf16 value.  Runs on the 128 threads of
-// the expansion warps.
+// the expansion warps; 9 chunks of 16 codes each.
 __device__ __forceinline__ void expand_e4m3_tile(uint32_t stage, int t) {
-  constexpr int kPer = kBoxesPerStage * 64 * 4 / 128;    // 16-value chunks per thread
+  constexpr int kPer = kFp8TileBytes / 16 / 128;
+  static_assert(kPer == 9, "8 latent chunks and 1 rope chunk per thread");
   uint4 v[kPer];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const int i = t + 128 * k;
     const int q = i & 3, r = (i >> 2) & 63, p = i >> 8;   // chunk in the row, row (key), box
     v[k] = lds128(stage + kFp8InPlace + p * kFp8Box + r * 64 + q * 16);
   }
+  // rope: row t >> 1, chunk t & 1
+  v[8] = lds128(stage + kFp8InPlace + kVBoxes * kFp8Box + (t >> 1) * 32 + (t & 1) * 16);
   named_bar_expand();
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const int i = t + 128 * k;
     const int q = i & 3, r = (i >> 2) & 63, p = i >> 8;
-    const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
     uint32_t o[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] & 0xFFFF), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] >> 16), __NV_E4M3);
-      const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-      const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-      o[2 * j] = pack_bf16x2(flo.x, flo.y);
-      o[2 * j + 1] = pack_bf16x2(fhi.x, fhi.y);
-    }
+    e4m3x16_to_bf16(v[k], o);
     const uint32_t row = stage + p * kBox + r * 128;
     sts128(row + (((2 * q) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
     sts128(row + (((2 * q + 1) ^ (r & 7)) << 4), o[4], o[5], o[6], o[7]);
+  }
+  {
+    const int r = t >> 1, q = t & 1;                      // 16 rope dims 16q.. of row r -> 64-B swizzled chunks 2q, 2q+1
+    uint32_t o[8];
+    e4m3x16_to_bf16(v[8], o);
+    const uint32_t row = stage + kRopeOff + r * 64;
+    const int sw = (r >> 1) & 3;
+    sts128(row + (((2 * q) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+    sts128(row + (((2 * q + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
   }
 }
 
 template <int kVariant>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 || kVariant == 3>::kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qpe,
-                  const __grid_constant__ CUtensorMap tm_kv, const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+                  const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kvr,
+                  const DecodeArgs a) {
   constexpr int kCacheFp8 = kVariant == 1 || kVariant == 3;
   constexpr bool kQ8 = kVariant == 3;       // e4m3 query: fp8 x fp8 score MMAs
   constexpr int kStages = Layout<kVariant>::kStages;
@@ -296,7 +383,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   const uint32_t peer = rank ^ 1u;
   const int cluster = (int)cluster_id_x();
   const Plan& P = a.plan;
-  Ctx ctx{bars, &P.header->status};
+  Ctx ctx{bars, &P.header->status, a.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -324,8 +411,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   }
   if (warp == R::kProducer && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_qpe);
+    tma_prefetch_desc(&tm_qr);
     tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_kvr);
   }
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised before any remote access
@@ -343,20 +431,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   auto producer = [&]() {
     // ------------------------------------------------------------ producer
     // Lane 0 streams everything with TMA: bf16 tiles straight into the ring;
-    // e4m3 tiles into the upper half of the ring slot, which the expansion warps turn into
-    // the bf16 ring slots the MMAs read.
+    // e4m3 tiles into the top of the ring slot, which the expansion warps
+    // turn into the bf16 layout the MMAs read.  Each CTA loads its 256
+    // latent columns [256r, 256r+256) and its 32 rope columns
+    // [512+32r, 512+32r+32) of every cached row.
     const bool leader = lane == 0;
     if (leader) {
       uint32_t item = 0;
       const int sub_rows = a.page_size < kTile ? a.page_size : kTile;
       const int nsub = kTile / sub_rows;
       const int oob_row = a.num_blocks * a.page_size;  // first row past the cache: reads zeros
+      const int xl = 256 * (int)rank, xr = kLkv + 32 * (int)rank;   // first latent / rope column of the CTA
       for (int u = ubeg; u < uend; ++u) {
         const UnitRec ur = P.units[u];
         const GroupRec gr = P.groups[ur.group];
         const int32_t* bt = a.block_table + (size_t)gr.b * a.max_pages;
-        // loads the CTA's 5 column boxes of tile j (all sub-pages) into dst, counting on `full`
-        auto load_tile = [&](int j, uint32_t dst, uint32_t full, int row_bytes) {
+        // loads the CTA's columns of tile j (all sub-pages) into dst, counting on `full`:
+        //   bf16:           4 latent boxes of 64 x 128 B, then the 64 x 64-B rope box
+        //   e4m3 (v1):      4 latent boxes of 64 x 64 B, then the 64 x 32-B rope box
+        //   e4m3 query (v3): 2 latent boxes of 64 x 128 B, then the 64 x 32-B rope box
+        auto load_tile = [&](int j, uint32_t dst, uint32_t full) {
           for (int sb = 0; sb < nsub; ++sb) {
             const int key = j * kTile + sb * sub_rows;
             const int lp = key / a.page_size;
@@ -368,30 +462,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
               else
                 atomicOr(ctx.status, 4);
             }
-            const int box_bytes = 64 * row_bytes;
-            for (int p = 0; p < kBoxesPerStage; ++p)
-              tma_load_2d(dst + p * box_bytes + sb * sub_rows * row_bytes, &tm_kv, 256 * rank + 64 * p, y, full);
-          }
-        };
-        // variant 3: the CTA's three 128-dim e4m3 boxes of tile j (128-B swizzle)
-        auto load_tile8 = [&](int j, uint32_t dst, uint32_t full) {
-          for (int sb = 0; sb < nsub; ++sb) {
-            const int key = j * kTile + sb * sub_rows;
-            const int lp = key / a.page_size;
-            int y = oob_row;
-            if (key < gr.lmax && lp < a.max_pages) {
-              const int blk = bt[lp];
-              if (blk >= 0 && blk < a.num_blocks)
-                y = blk * a.page_size + key % a.page_size;
-              else
-                atomicOr(ctx.status, 4);
+            if constexpr (kQ8) {
+              for (int p = 0; p < 2; ++p)
+                tma_load_2d(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, y, full);
+              tma_load_2d(dst + 2 * kQ8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full);
+            } else if constexpr (kCacheFp8) {
+              for (int p = 0; p < kVBoxes; ++p)
+                tma_load_2d(dst + p * kFp8Box + sb * sub_rows * 64, &tm_kv, xl + 64 * p, y, full);
+              tma_load_2d(dst + kVBoxes * kFp8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full);
+            } else {
+              for (int p = 0; p < kVBoxes; ++p)
+                tma_load_2d(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, y, full);
+              tma_load_2d(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, y, full);
             }
-            for (int p = 0; p < kQ8Boxes; ++p)
-              tma_load_2d(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, 256 * rank + 128 * p, y, full);
           }
         };
         const int ntiles = ur.tile_end - ur.tile_begin;
-        // the CTA's 288 query dims (5 boxes of 64) for rows 0-63, then 64-127
+        // the CTA's 288 query dims for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
           if (!leader) continue;
           const uint32_t slot = item % kStages, round = item / kStages;
@@ -399,45 +486,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
           const int y = gr.row0 + 64 * half;
           if constexpr (kQ8) {
-            // e4m3 query rows [q_abs | q_pe] (576 wide): the CTA's three
-            // 128-dim boxes; the last box of CTA 1 runs past dim 575 (zeros)
+            // e4m3 query rows [q_abs | q_pe] (576 wide): the CTA's two
+            // 128-dim latent boxes and its 32-dim rope box
             const uint32_t full = smem_u32(&bars->stg_full[slot]);
             mbar_expect_tx(full, kQ8Bytes);
-            for (int p = 0; p < kQ8Boxes; ++p)
-              tma_load_2d(st + kQ8InPlace + p * kQ8Box, &tm_q, 256 * rank + 128 * p, y, full);
+            for (int p = 0; p < 2; ++p) tma_load_2d(st + kQ8InPlace + p * kQ8Box, &tm_q, xl + 128 * p, y, full);
+            tma_load_2d(st + kQ8InPlace + 2 * kQ8Box, &tm_qr, xr, y, full);
             // kv_full's phases count every item of the slot
             mbar_arrive(smem_u32(&bars->kv_full[slot]));
           } else {
+            // bf16 q_abs boxes (64 dims) and the q_pe half (32 dims, 64-B swizzle)
             const uint32_t full = smem_u32(&bars->kv_full[slot]);
             mbar_expect_tx(full, kStageBytes);
-            for (int p = 0; p < kBoxesPerStage; ++p) {
-              if (rank == 1 && p == 4)
-                tma_load_2d(st + p * kBox, &tm_qpe, 0, y, full);
-              else
-                tma_load_2d(st + p * kBox, &tm_q, 256 * rank + 64 * p, y, full);
-            }
+            for (int p = 0; p < kVBoxes; ++p) tma_load_2d(st + p * kBox, &tm_q, xl + 64 * p, y, full);
+            tma_load_2d(st + kRopeOff, &tm_qr, 32 * (int)rank, y, full);
             // e4m3 cache: a query item also completes a phase of the slot's
             // stg_full, so its phases count every item of the slot
             if (kCacheFp8) mbar_arrive(smem_u32(&bars->stg_full[slot]));
           }
         }
         for (int jj = 0; jj < ntiles; ++jj, ++item) {
+          // test aid: CTA 0 of cluster 0 never loads its first cache tile, so
+          // a consumer's bounded wait for it runs out
+          if (a.debug_skip_tile && cluster == 0 && rank == 0 && u == ubeg && jj == 0) continue;
           const uint32_t slot = item % kStages, round = item / kStages;
-          if (!kCacheFp8) {
-            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+          wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+          if constexpr (!kCacheFp8) {
             const uint32_t full = smem_u32(&bars->kv_full[slot]);
             mbar_expect_tx(full, kStageBytes);
-            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full, 128);
+            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full);
           } else if constexpr (kQ8) {
-            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
             const uint32_t full = smem_u32(&bars->stg_full[slot]);
             mbar_expect_tx(full, kQ8Bytes);
-            load_tile8(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kQ8InPlace), full);
+            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kQ8InPlace), full);
           } else {
-            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
             const uint32_t full = smem_u32(&bars->stg_full[slot]);
             mbar_expect_tx(full, kFp8TileBytes);
-            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kFp8InPlace), full, 64);
+            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kFp8InPlace), full);
           }
         }
       }
@@ -446,7 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       if (leader) {
         const uint32_t first = item > kStages ? item - kStages : 0;
         for (uint32_t k = first; k < item; ++k)
-          mbar_wait(smem_u32(kQ8 ? &bars->stg_full[k % kStages] : &bars->kv_full[k % kStages]), (k / kStages) & 1);
+          mbar_wait(smem_u32(kQ8 ? &bars->stg_full[k % kStages] : &bars->kv_full[k % kStages]), (k / kStages) & 1,
+                    a.wait_limit_ns);
       }
     }
     __syncwarp();
@@ -455,10 +541,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     // ---------------------------------------------------- score-MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, kTile, 0, 0);   // K-major keys, N = 64
-      const uint64_t kv_desc0 = smem_desc(smem_u32(stages), 16, 1024, kSwizzle128B);
       constexpr uint64_t kStageDesc = kStageBytes >> 4;
+      // latent boxes: 128-B swizzle, 8-row groups 1024 B apart; rope box:
+      // 64-B swizzle, 8-row groups 512 B apart
+      const uint64_t kv_desc0 = smem_desc(smem_u32(stages), 16, 1024, kSwizzle128B);
+      const uint64_t kr_desc0 = smem_desc(smem_u32(stages + kRopeOff), 16, 512, kSwizzle64B);
       const uint32_t d = tbase + kTmemS;
-      const uint32_t qa = tbase + kTmemQ - 16 * rank;     // column of (box p, step k) = p*32 + k*8 - 16*rank
+      const uint32_t qa = tbase + kTmemQ;      // latent box p, 16-dim step k: column p*32 + k*8; rope: 128 + k*8
       uint32_t item = 0, it = 0, units_done = 0;
       for (int u = ubeg; u < uend; ++u, ++units_done) {
         const UnitRec ur = P.units[u];
@@ -475,20 +564,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           const uint32_t slot = item % kStages, round = item / kStages;
           if constexpr (kQ8) {
             // fp8 x fp8: the e4m3 boxes are read as they landed, 9 MMAs of K = 32
+            // (8 over the two 128-dim latent boxes, 1 over the 32-dim rope box)
             wait_bar(ctx, &bars->stg_full[slot], round & 1);
             wait_bar(ctx, &bars->s_free, (it & 1) ^ 1);
             tc_fence_after();
             constexpr uint32_t id_s8 = idesc_e4m3_f32(128, kTile);
-            const uint64_t kd8 = smem_desc(smem_u32(stages + slot * kStageBytes + kQ8InPlace), 16, 1024, kSwizzle128B);
-            uint32_t j = 0;
+            const uint32_t base8 = smem_u32(stages + slot * kStageBytes + kQ8InPlace);
+            const uint64_t kd8 = smem_desc(base8, 16, 1024, kSwizzle128B);
+            const uint64_t kr8 = smem_desc(base8 + 2 * kQ8Box, 16, 256, kSwizzle32B);
 #pragma unroll
-            for (int p = 0; p < kQ8Boxes; ++p)
+            for (int p = 0; p < 2; ++p)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                if (kstep8_valid(rank, p, k)) {
-                  mma_ts_f8(d, tbase + kTmemQ + 8 * j, kd8 + ((p * kQ8Box + k * 32) >> 4), id_s8, j > 0 ? 1u : 0u);
-                  ++j;
-                }
+                mma_ts_f8(d, qa + 32 * p + 8 * k, kd8 + ((p * kQ8Box + k * 32) >> 4), id_s8, (p | k) ? 1u : 0u);
+            mma_ts_f8(d, qa + 64, kr8, id_s8, 1u);
             mma_commit(smem_u32(&bars->s_full));
             mma_commit(smem_u32(&bars->kv_empty[slot]));
             mma_commit(smem_u32(&bars->kx_free[slot]));
@@ -498,21 +587,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           wait_bar(ctx, &bars->s_free, (it & 1) ^ 1);
           tc_fence_after();
           const uint64_t kd = kv_desc0 + slot * kStageDesc;
-          bool first = true;
+          const uint64_t kr = kr_desc0 + slot * kStageDesc;
 #pragma unroll
-          for (int p = 0; p < kBoxesPerStage; ++p)
+          for (int p = 0; p < kVBoxes; ++p)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              if (kstep_valid(rank, p, k)) {
-                mma_ts(d, qa + p * 32 + k * 8, kd + ((p * kBox + k * 32) >> 4), id_s, first ? 0u : 1u);
-                first = false;
-              }
+              mma_ts(d, qa + p * 32 + k * 8, kd + ((p * kBox + k * 32) >> 4), id_s, (p | k) ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) mma_ts(d, qa + 128 + k * 8, kr + ((k * 32) >> 4), id_s, 1u);
           mma_commit(smem_u32(&bars->s_full));
           mma_commit(smem_u32(&bars->kv_empty[slot]));
         }
       }
       mma_commit(smem_u32(&bars->s_drain));
-      mbar_wait(smem_u32(&bars->s_drain), 0);
+      mbar_wait(smem_u32(&bars->s_drain), 0, a.wait_limit_ns);
     }
     __syncwarp();
   };
@@ -544,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         mma_commit(smem_u32(&bars->o_full));
       }
       mma_commit(smem_u32(&bars->p_drain));
-      mbar_wait(smem_u32(&bars->p_drain), 0);
+      mbar_wait(smem_u32(&bars->p_drain), 0, a.wait_limit_ns);
     }
     __syncwarp();
   };
@@ -560,10 +648,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         const uint32_t slot = item % kStages, round = item / kStages;
         wait_bar(ctx, &bars->stg_full[slot], round & 1);
         if constexpr (kQ8) {
-          // Variant 3: the value dims (e4m3 boxes 0-1 = the CTA's 256 output
-          // dims) become the bf16 boxes 0-3 of the slot, which overlap e4m3
-          // boxes 0-1: read everything, wait until the tile's score MMAs are
-          // done with the e4m3 boxes, then write.
+          // Variant 3: the value dims (the two 128-dim e4m3 boxes = the CTA's
+          // 256 output dims) become the bf16 boxes 0-3 of the slot, which
+          // overlap the e4m3 boxes: read everything, wait until the tile's
+          // score MMAs are done with the e4m3 boxes, then write.
           const uint32_t st = smem_u32(stages + slot * kStageBytes);
           uint4 v[8];
 #pragma unroll
@@ -579,17 +667,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
             const int i = te + 128 * k;
             const int q = i & 7, r = (i >> 3) & 63, b = i >> 9;
             // 16 values: output dims 128 b + 16 q + [0, 16) -> bf16 box 2b + q/4, chunks 2(q%4), 2(q%4)+1
-            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
             uint32_t o[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] & 0xFFFF), __NV_E4M3);
-              const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[j] >> 16), __NV_E4M3);
-              const float2 flo = __half22float2(*reinterpret_cast<const __half2*>(&lo));
-              const float2 fhi = __half22float2(*reinterpret_cast<const __half2*>(&hi));
-              o[2 * j] = pack_bf16x2(flo.x, flo.y);
-              o[2 * j + 1] = pack_bf16x2(fhi.x, fhi.y);
-            }
+            e4m3x16_to_bf16(v[k], o);
             const uint32_t rowa = st + (2 * b + (q >> 2)) * kBox + r * 128;
             const int c0 = 2 * (q & 3);
             sts128(rowa + ((c0 ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
@@ -615,7 +694,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     // receive buffers are chunk-major, [8][kXRows][16 B]: the 32 lanes of a
     // warp write (and read) 512 contiguous bytes per instruction
     const uint32_t xrow = (uint32_t)row * 16;
-    constexpr uint32_t kXChunk = (uint32_t)kXRows * 16;
+    constexpr uint32_t kXChunk = (uint32_t)Layout<kVariant>::kXChunk;
+    constexpr uint32_t kXHdr = (uint32_t)Layout<kVariant>::kXHdr;
     const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
@@ -638,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         dst[32 + c] = __uint_as_float(r1[c]);
       }
       if constexpr (kQ8) {
-        // sums of code products -> real partial scores before the fp16 exchange
+        // sums of code products -> real partial scores (both halves in the same units)
 #pragma unroll
         for (int c = 0; c < kTile; ++c) dst[c] *= a.qk_scale;
       }
@@ -646,42 +726,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
     };
-    // Send partial scores of tile `t` (fp16, valid rows only) straight into the
-    // peer's receive buffer: 16-byte st.async stores that count against the
+    // Send partial scores of tile `t` (valid rows only) straight into the
+    // peer's receive buffer as 16-bit block fixed point: codes of (s - c) /
+    // step over the keys the row may see (`nvis` of the tile's 64), then the
+    // row header (c, step).  16-byte st.async stores that count against the
     // peer's barrier (this keeps the exchange off the TMA engine that streams
     // the cache tiles).
-    auto send_s = [&](uint32_t t, const float (&src)[kTile]) {
+    auto send_s = [&](uint32_t t, const float (&src)[kTile], int nvis) {
       const uint32_t b = t % kXBuffers;
       if (row < nrows_cur) {
+        float hi, lo;
+        range64(src, nvis, hi, lo);
+        if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this tile
+        const float ctr = 0.5f * (hi + lo);
+        // |fl(s - ctr)| <= half for every s in [lo, hi] (monotone rounding)
+        const float half = fmaxf(fmaxf(hi - ctr, ctr - lo), 1e-30f);
+        const float step = half * (1.f / kCodeRange);
+        const float inv = __fdividef(kCodeRange, half);
         const uint32_t base = xrecv_peer0 + b * kXBytes + xrow;
         const uint32_t bar = xfull_peer0 + b * 8;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(base + c * kXChunk, pack_f16x2(src[8 * c], src[8 * c + 1]),
-                      pack_f16x2(src[8 * c + 2], src[8 * c + 3]), pack_f16x2(src[8 * c + 4], src[8 * c + 5]),
-                      pack_f16x2(src[8 * c + 6], src[8 * c + 7]), bar);
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float d0 = src[8 * c + 2 * j], d1 = src[8 * c + 2 * j + 1];
+            add2(d0, d1, -ctr, -ctr);
+            float f0, f1;
+            fma2(f0, f1, d0, d1, inv, kCodeMagic);      // rounds to the integer code + 32768
+            w[j] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
+          }
+          st_async_v4(base + c * kXChunk, w[0], w[1], w[2], w[3], bar);
+        }
+        st_async_v2(xrecv_peer0 + b * kXBytes + kXHdr + (uint32_t)row * 8, __float_as_uint(ctr),
+                    __float_as_uint(step), bar);
       }
     };
-    // Add the peer's partial scores of tile `t` into `acc`.
-    auto recv_s = [&](uint32_t t, float (&acc)[kTile], uint32_t nbytes) {
+    // Add the peer's partial scores of tile `t`, less the row's centre c, into
+    // `acc`; returns c (the caller folds it into the maximum and the exponent).
+    auto recv_s = [&](uint32_t t, float (&acc)[kTile], uint32_t nbytes) -> float {
       const uint32_t b = t % kXBuffers, use = t / kXBuffers;
       if (tid128 == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
       wait_bar_cluster(ctx, &bars->x_full[b], use & 1);
       __syncwarp();
-      const uint32_t base = xrecv0 + b * kXBytes + xrow;
+      float ctr = 0.f;
+      if (row < kXRows) {
+        const uint2 h = lds64(xrecv0 + b * kXBytes + kXHdr + (uint32_t)row * 8);
+        ctr = __uint_as_float(h.x);
+        const float step = __uint_as_float(h.y);
+        const uint32_t base = xrecv0 + b * kXBytes + xrow;
 #pragma unroll
-      for (int c = 0; c < 8 && row < kXRows; ++c) {
-        const uint4 v = lds128(base + c * kXChunk);
-        const float2 f0 = unpack_f16x2(v.x), f1 = unpack_f16x2(v.y), f2 = unpack_f16x2(v.z), f3 = unpack_f16x2(v.w);
-        add2(acc[8 * c + 0], acc[8 * c + 1], f0.x, f0.y);
-        add2(acc[8 * c + 2], acc[8 * c + 3], f1.x, f1.y);
-        add2(acc[8 * c + 4], acc[8 * c + 5], f2.x, f2.y);
-        add2(acc[8 * c + 6], acc[8 * c + 7], f3.x, f3.y);
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = lds128(base + c * kXChunk);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float f0 = __uint_as_float(__byte_perm(w[j], 0x4B40u, 0x5410));   // 12582912 + u
+            float f1 = __uint_as_float(__byte_perm(w[j], 0x4B40u, 0x5432));
+            add2(f0, f1, -kCodeMagic, -kCodeMagic);                           // the code, exactly
+            fma2v(acc[8 * c + 2 * j], acc[8 * c + 2 * j + 1], f0, f1, step);
+          }
+        }
       }
       // every row of buffer b is read before any thread sends its row of a
       // later tile: a received tile then proves the peer is done with the
       // buffer three tiles back, whatever the row counts of the units
       named_bar_softmax();
+      return ctr;
     };
 
     uint32_t item = 0, it = 0, units_done = 0;
@@ -704,31 +815,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       }
       // the warp needs masking only on tiles that reach past its shortest valid row
       const int lmin_warp = __reduce_min_sync(0xffffffffu, Lr);
-      const uint32_t nbytes = (uint32_t)gr.nrows * (kTile * 2);
+      const uint32_t nbytes = (uint32_t)gr.nrows * kXRowBytes;
 
       // the CTA's 288 query dims -> TMEM (A operand of the score MMAs)
       if constexpr (kQ8) {
-        // e4m3 query: the nine 32-dim K steps of the CTA's 288 dims, four
-        // codes per TMEM column, in the order the score issuer walks them
+        // e4m3 query: the nine 32-dim K steps of the CTA's 288 dims (eight
+        // from its two 128-dim latent boxes, one from its 32-dim rope box),
+        // four codes per TMEM column, in the order the score issuer walks them
         const uint32_t my = item + (row >= 64 ? 1 : 0);
         wait_bar(ctx, &bars->stg_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
         const int k = row & 63;
-        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + kQ8InPlace + k * 128;
+        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + kQ8InPlace;
         const uint32_t sgn = a.neg_q ? 0x80808080u : 0u;   // a negative scale negates q
-        uint32_t j = 0;
 #pragma unroll
-        for (int p = 0; p < kQ8Boxes; ++p)
+        for (int p = 0; p < 2; ++p)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            if (kstep8_valid(rank, p, kk)) {
-              const uint4 v0 = lds128(base + p * kQ8Box + (((2 * kk) ^ (k & 7)) << 4));
-              const uint4 v1 = lds128(base + p * kQ8Box + (((2 * kk + 1) ^ (k & 7)) << 4));
-              const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
-                                     v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
-              tmem_st8(tl + kTmemQ + 8 * j, w);
-              ++j;
-            }
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint4 v0 = lds128(base + p * kQ8Box + k * 128 + (((2 * kk) ^ (k & 7)) << 4));
+            const uint4 v1 = lds128(base + p * kQ8Box + k * 128 + (((2 * kk + 1) ^ (k & 7)) << 4));
+            const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
+                                   v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
+            tmem_st8(tl + kTmemQ + 32 * p + 8 * kk, w);
+          }
+        {
+          // rope box: 32-byte rows, 32-B swizzle (16-byte chunk c of row k at c ^ ((k >> 2) & 1))
+          const uint32_t rb = base + 2 * kQ8Box + k * 32;
+          const int sw = (k >> 2) & 1;
+          const uint4 v0 = lds128(rb + ((0 ^ sw) << 4));
+          const uint4 v1 = lds128(rb + ((1 ^ sw) << 4));
+          const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
+                                 v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
+          tmem_st8(tl + kTmemQ + 64, w);
+        }
         tmem_wait_st();
         tc_fence_before();
         named_bar_softmax();
@@ -745,32 +864,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         wait_bar(ctx, &bars->kv_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
         const int k = row & 63;
-        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + k * 128;
+        const uint32_t sbase = smem_u32(stages + (my % kStages) * kStageBytes);
+        const uint32_t sgn = a.neg_q ? 0x80008000u : 0u;   // a negative scale negates q
 #pragma unroll
-        for (int p = 0; p < kBoxesPerStage; ++p) {
+        for (int p = 0; p < kVBoxes; ++p) {
           uint32_t q[32];
-          const uint32_t sgn = a.neg_q ? 0x80008000u : 0u;   // a negative scale negates q
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 v = lds128(base + p * kBox + ((c ^ (k & 7)) << 4));
+            const uint4 v = lds128(sbase + p * kBox + k * 128 + ((c ^ (k & 7)) << 4));
             q[4 * c + 0] = v.x ^ sgn;
             q[4 * c + 1] = v.y ^ sgn;
             q[4 * c + 2] = v.z ^ sgn;
             q[4 * c + 3] = v.w ^ sgn;
           }
-          if (rank == 0 && p == 4) {
-            uint32_t h[16];
+          tmem_st32(tl + kTmemQ + p * 32, q);
+        }
+        {
+          // q_pe half: 64-byte rows, 64-B swizzle (chunk c of row k at c ^ ((k >> 1) & 3))
+          uint32_t h[16];
+          const int sw = (k >> 1) & 3;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) h[c] = q[c];                    // dims 256-287
-            tmem_st16(tl + kTmemQ + 128, h);
-          } else if (rank == 1 && p == 0) {
-            uint32_t h[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) h[c] = q[16 + c];               // dims 288-319
-            tmem_st16(tl + kTmemQ, h);
-          } else {
-            tmem_st32(tl + kTmemQ + p * 32 - 16 * rank, q);
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = lds128(sbase + kRopeOff + k * 64 + ((c ^ sw) << 4));
+            h[4 * c + 0] = v.x ^ sgn;
+            h[4 * c + 1] = v.y ^ sgn;
+            h[4 * c + 2] = v.z ^ sgn;
+            h[4 * c + 3] = v.w ^ sgn;
           }
+          tmem_st16(tl + kTmemQ + 128, h);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -787,18 +908,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
 
       float m = -INFINITY, l = 0.f;
       const int ntiles = ur.tile_end - ur.tile_begin;
+      // keys of tile jj the row may see (64 on every tile before its last)
+      auto nvis = [&](int jj) { return Lr - (ur.tile_begin + jj) * kTile; };
       float cur[kTile], nxt[kTile];
       if (ntiles > 0) {
         load_s(it, cur);
-        send_s(it, cur);
+        send_s(it, cur, nvis(0));
       }
       for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
         // exchange of the next tile first: the network copy overlaps this tile's work
         if (jj + 1 < ntiles) {
           load_s(it + 1, nxt);
-          send_s(it + 1, nxt);
+          send_s(it + 1, nxt, nvis(jj + 1));
         }
-        recv_s(it, cur, nbytes);
+        const float cpeer = recv_s(it, cur, nbytes);   // cur = own + peer partial - cpeer
 
         // mask on ragged tiles, tree max of the unscaled scores (the scale is
         // positive), then exp2(scale * s - m) as one FMA into the exponential
@@ -807,15 +930,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
 #pragma unroll
           for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
         }
-        float mx[22];
-#pragma unroll
-        for (int c = 0; c < 21; ++c) mx[c] = fmax3(cur[3 * c], cur[3 * c + 1], cur[3 * c + 2]);
-        mx[21] = cur[63];
-#pragma unroll
-        for (int c = 0; c < 7; ++c) mx[c] = fmax3(mx[3 * c], mx[3 * c + 1], mx[3 * c + 2]);
-        mx[7] = mx[21];
-        const float tmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) *
-                           a.scale_log2;
+        const float tmax = (max64(cur) + cpeer) * a.scale_log2;
         float alpha = 1.f;
         if (valid && tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
@@ -823,12 +938,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           m = tmax;
         }
         const float mref = m == -INFINITY ? 0.f : m;
+        const float kexp = fmaf(cpeer, a.scale_log2, -mref);   // exponent offset of the row
         uint32_t pk[kTile / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kTile / 2; ++c) {
           float x0, x1;
-          fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, -mref);
+          fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, kexp);
           const float p0 = fast_exp2(x0);
           const float p1 = fast_exp2(x1);
           add2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], p0, p1);
@@ -961,8 +1077,9 @@ size_t decode_smem_bytes(int variant) {
                       : (variant == 2 ? smem_bytes<2>() : (variant == 3 ? smem_bytes<3>() : smem_bytes<0>()));
 }
 
-cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, const CUtensorMap& tm_kv, int variant,
-                          const DecodeArgs& a, int num_clusters, cudaStream_t s) {
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
+                          const CUtensorMap& tm_kvr, int variant, const DecodeArgs& a, int num_clusters,
+                          cudaStream_t s) {
   const size_t smem = decode_smem_bytes(variant);
   auto kern = variant == 1 ? decode_kernel<1>
                            : (variant == 2 ? decode_kernel<2> : (variant == 3 ? decode_kernel<3> : decode_kernel<0>));
@@ -980,7 +1097,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qpe, co
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qpe, tm_kv, a);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qr, tm_kv, tm_kvr, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -1,8 +1,8 @@
 // Thin inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
 // tcgen05 (TMEM alloc / MMA / ld / st / commit) and cluster shared memory.
-// Every wait is bounded: it gives up after MLA_WAIT_LIMIT_NS of wall time and
-// reports failure to the caller, which raises the kernel's error flag and
-// unwinds instead of hanging the GPU.
+// Every wait is bounded: it gives up after a wall-time limit (MLA_WAIT_LIMIT_NS
+// unless the caller passes its own) and reports failure to the caller, which
+// raises the kernel's error flag and unwinds instead of hanging the GPU.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -91,7 +91,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // the thread for a hardware-chosen interval): fewer polls of shared memory
 // leave more of it to the SM-to-SM traffic of the decode kernel (measured:
 // 14 % faster on a 16-head, long-context batch).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = MLA_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -99,17 +99,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
       if (mbar_try_wait(bar, parity)) return true;
       __nanosleep(256);
     }
-    if (globaltimer() - t0 > MLA_WAIT_LIMIT_NS) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = MLA_WAIT_LIMIT_NS) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (globaltimer() - t0 > MLA_WAIT_LIMIT_NS) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -189,6 +190,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote, uint32_t a, uint32_
       : "memory");
 }
 
+// 8-byte variant of st_async_v4.
+__device__ __forceinline__ void st_async_v2(uint32_t remote, uint32_t a, uint32_t b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(remote),
+               "r"(a), "r"(b), "r"(remote_bar)
+               : "memory");
+}
+
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into a
 // peer CTA's shared memory, completing `bytes` of transaction count on the
 // peer's mbarrier.  Both addresses 16-byte aligned.
@@ -254,6 +262,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle64B = 4;
+constexpr uint32_t kSwizzle32B = 6;
 
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
