@@ -62,9 +62,10 @@ enum mla_device_error {
 
 /*
  * mla_cache_write -- concat_and_cache_mla: store the latent rows of new tokens
- * in the paged cache (common.py, MLACommonImpl.forward, "write the latent and
- * rope to kv cache"; mla_attention.py, MLAAttention.forward ->
- * do_kv_cache_update).
+ * in the paged cache (page "vllm/v1/attention/backends/mla/common.py",
+ * MLACommonImpl.forward, the cache update before the attention; page
+ * "vllm.model_executor.layers.attention.mla_attention", MLAAttention.forward
+ * and do_kv_cache_update).
  *
  *   kv_c          [num_tokens, 512] bf16, 16-byte aligned
  *   k_pe          [num_tokens, 64]  bf16, 16-byte aligned
@@ -208,7 +209,7 @@ MLA_API int mla_set_decode_timing_events(void* start, void* stop);
  * All calls share the one array and it keeps the last call's contents, so
  * calls that may overlap on the GPU (different streams, different host
  * threads) race: serialise them on one stream.  The device error word of
- * these calls lives in the shared array and is not exposed.
+ * these calls lives in the shared array; mla_decode_no_alloc_status reads it.
  */
 #define MLA_NO_ALLOC_SCRATCH_BYTES ((size_t)96 << 20)
 MLA_API int mla_decode_no_alloc(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks,
@@ -218,10 +219,22 @@ MLA_API int mla_decode_no_alloc(const void* q_abs, const void* q_pe, const void*
                                 int num_splits, void* out, float* lse, void* stream);
 
 /*
- * mla_q_absorb -- query absorption of the decode branch (common.py,
- * MLACommonImpl.forward: "Multiply (N, B, P) x (N, P, L) -> (N, B, L)",
- * torch.bmm(decode_q_nope, self.W_UK_T); the docstring's
- * ql_nope = einsum("snp,lnp->snl", q_nope, W_UK)):
+ * mla_decode_no_alloc_status -- the device error word (OR of mla_device_error
+ * bits; 0 = clean) of the last mla_decode_no_alloc on the current device,
+ * copied to *status; cleared afterwards if `clear` is non-zero.  Like
+ * mla_decode_no_alloc it has no counterpart on the pages: it gives the
+ * callers that cannot allocate the same view of bad block-table entries,
+ * bad sequence lengths and expired on-chip waits that mla_decode_status gives
+ * workspace callers.  Synchronises `stream`; allocates nothing.
+ */
+MLA_API int mla_decode_no_alloc_status(int* status, int clear, void* stream);
+
+/*
+ * mla_q_absorb -- query absorption of the decode branch (page
+ * "vllm/v1/attention/backends/mla/common.py", MLACommonImpl.forward: the
+ * no-rope part of every head's query is multiplied by that head's W_UK_T with
+ * a batched matmul over heads; the module docstring's ql_nope in the
+ * "Data-Movement Friendly Approach"):
  *
  *   ql_nope[t, n, l] = sum_p q_nope[t, n, p] * w_uk_t[n, p, l]
  *
@@ -245,9 +258,11 @@ MLA_API int mla_q_absorb(const void* q_nope, int64_t q_row_stride, const void* w
                          int num_heads, int nope_dim, void* ql_nope, void* stream);
 
 /*
- * mla_v_up_proj -- the value up-projection after the latent decode (common.py,
- * MLACommonBaseImpl._v_up_proj: "Multiply (N, B, L) x (N, L, V) -> (N, B, V)",
- * torch.bmm(x, self.W_UV); the docstring's einsum("snl,lnv->snv", o, W_UV)):
+ * mla_v_up_proj -- the value up-projection after the latent decode (page
+ * "vllm/v1/attention/backends/mla/common.py", MLACommonBaseImpl._v_up_proj:
+ * every head's latent output is multiplied by that head's W_UV with a batched
+ * matmul over heads; the module docstring's last step of the "Data-Movement
+ * Friendly Approach"):
  *
  *   out[t, n, v] = sum_l o_lat[t, n, l] * w_uv[n, l, v]
  *
@@ -350,6 +365,20 @@ MLA_API int mla_gather_cache(const void* cache, int64_t num_blocks, int page_siz
                              const int32_t* block_table, int max_pages_per_seq, const int32_t* cu_seq_lens,
                              const int32_t* seq_starts, int batch, void* dst, int64_t num_tokens, int32_t* status,
                              void* stream);
+
+/*
+ * mla_set_decode_wait_test -- test aid for the failure detection of the
+ * decode kernels (the pages have no counterpart).  Every mbarrier wait inside
+ * a decode is bounded in wall time; when one runs out, the CTA records
+ * MLA_DEVERR_TIMEOUT in the device error word and unwinds without hanging.
+ * After this call, later mla_decode / mla_decode_fp8q / mla_decode_no_alloc
+ * calls of the calling thread bound every wait by `wait_limit_ns` (0 = the
+ * default 1 s; otherwise 1e5..1e9), and with skip_first_tile != 0 the first
+ * CTA of the grid never loads its first cache tile, so the wait for that tile
+ * runs out.  The decode still returns; its outputs are then undefined and the
+ * error word reports the timeout.  Call with (0, 0) to restore the defaults.
+ */
+MLA_API int mla_set_decode_wait_test(int skip_first_tile, unsigned long long wait_limit_ns);
 
 /* Human-readable description of the calling thread's last error ("" if none). */
 MLA_API const char* mla_last_error(void);

@@ -29,7 +29,8 @@ DQK = 576
 C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "mla_decode_status",
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
                  "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
-                 "mla_gather_cache", "mla_quantize_fp8", "mla_decode_fp8q")
+                 "mla_gather_cache", "mla_quantize_fp8", "mla_decode_fp8q", "mla_set_decode_wait_test",
+                 "mla_decode_no_alloc_status")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -80,6 +81,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_gather_cache.argtypes = [P, i64, i32, i32, f32, P, i32, P, P, i32, P, i64, P, P]
     lib.mla_proj_status.restype = i32
     lib.mla_proj_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
+    lib.mla_set_decode_wait_test.restype = i32
+    lib.mla_set_decode_wait_test.argtypes = [i32, ctypes.c_ulonglong]
+    lib.mla_decode_no_alloc_status.restype = i32
+    lib.mla_decode_no_alloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
     _lib = lib
     return lib
 
@@ -116,11 +121,43 @@ def _dtype_code(cache):
     raise TypeError(f"cache dtype {cache.dtype} is neither bf16 nor float8_e4m3fn")
 
 
+def _dense(t, name: str, dtypes, shape=None, dims=None):
+    """Refuse a tensor the library would misread: the C ABI takes dense
+    row-major tensors of fixed element types.  ``shape`` entries of None
+    match any size; ``dims`` checks only the rank."""
+    import torch
+    if not isinstance(dtypes, tuple):
+        dtypes = (dtypes,)
+    if t.dtype not in dtypes:
+        want = " or ".join(str(d).replace("torch.", "") for d in dtypes)
+        raise ValueError(f"{name} must be {want}, got {str(t.dtype).replace('torch.', '')}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got shape {tuple(t.shape)}")
+    if shape is not None:
+        if t.dim() != len(shape) or any(w is not None and int(n) != w for n, w in zip(t.shape, shape)):
+            exp = "[" + ", ".join("*" if w is None else str(w) for w in shape) + "]"
+            raise ValueError(f"{name} must have shape {exp}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (dense rows), got strides {t.stride()}")
+    del torch
+
+
+def _cache_checked(cache, name="cache"):
+    import torch
+    _dense(cache, name, (torch.bfloat16, torch.float8_e4m3fn, torch.uint8), dims=3)
+    if cache.shape[2] != DQK:
+        raise ValueError(f"cache rows must be {DQK} wide, got {cache.shape[2]}")
+    return cache.shape
+
+
 def cache_write(kv_c, k_pe, slot_mapping, cache, kv_scale: float = 1.0, stream=None) -> None:
     """concat_and_cache_mla: cache[num_blocks, page, 576] (bf16 or float8_e4m3fn)."""
-    nb, ps, w = cache.shape
-    if w != DQK:
-        raise ValueError(f"cache rows must be {DQK} wide, got {w}")
+    import torch
+    nb, ps, _ = _cache_checked(cache)
+    _dense(slot_mapping, "slot_mapping", torch.int64, dims=1)
+    T = slot_mapping.numel()
+    _dense(kv_c, "kv_c", torch.bfloat16, (T, LKV))
+    _dense(k_pe, "k_pe", torch.bfloat16, (T, ROPE))
     _check(load().mla_cache_write(_ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), slot_mapping.numel(), _ptr(cache),
                                   nb, ps, _dtype_code(cache), float(kv_scale), _stream(stream)))
 
@@ -133,12 +170,37 @@ def decode(q_abs, q_pe, cache, block_table, seq_lens, out, workspace, *, scale: 
            query_start_loc=None, lse=None, num_splits: int = 0, kv_scale: float = 1.0, stream=None) -> None:
     """Absorbed MLA decode (forward_mqa) into ``out`` [T, N, 512] bf16 and ``lse`` [T, N] fp32."""
     T, N, _ = q_abs.shape
-    nb, ps, _ = cache.shape
+    nb, ps, _ = _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse)
+    _dense(workspace, "workspace", (workspace.dtype,))
     B = seq_lens.numel()
     _check(load().mla_decode(_ptr(q_abs), _ptr(q_pe), _ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale),
                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
                              T, N, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse, q8=None):
+    """Validate the dense tensors of a decode call; returns the cache shape."""
+    import torch
+    if q8 is None:
+        _dense(q_abs, "q_abs", torch.bfloat16, (None, None, LKV))
+        T, N, _ = q_abs.shape
+        _dense(q_pe, "q_pe", torch.bfloat16, (T, N, ROPE))
+    else:
+        _dense(q8, "q_fp8", (torch.uint8, torch.float8_e4m3fn), (None, None, DQK))
+        T, N, _ = q8.shape
+    shape = _cache_checked(cache)
+    _dense(block_table, "block_table", torch.int32, dims=2)
+    _dense(seq_lens, "seq_lens", torch.int32, dims=1)
+    B = seq_lens.numel()
+    if block_table.shape[0] != B:
+        raise ValueError(f"block_table must have one row per request ({B}), got {block_table.shape[0]}")
+    if query_start_loc is not None:
+        _dense(query_start_loc, "query_start_loc", torch.int32, (B + 1,))
+    _dense(out, "out", torch.bfloat16, (T, N, LKV))
+    if lse is not None:
+        _dense(lse, "lse", torch.float32, (T, N))
+    return shape
 
 
 def decode_no_alloc(q_abs, q_pe, cache, block_table, seq_lens, out, *, scale: float, query_start_loc=None,
@@ -147,7 +209,7 @@ def decode_no_alloc(q_abs, q_pe, cache, block_table, seq_lens, out, *, scale: fl
     library's own fixed 96 MiB device array (shared by all calls; calls that
     overlap on the GPU race).  Batches needing more scratch raise MLAError."""
     T, N, _ = q_abs.shape
-    nb, ps, _ = cache.shape
+    nb, ps, _ = _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse)
     B = seq_lens.numel()
     _check(load().mla_decode_no_alloc(_ptr(q_abs), _ptr(q_pe), _ptr(cache), nb, ps, _dtype_code(cache),
                                       float(kv_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
@@ -160,7 +222,8 @@ def decode_fp8q(q_fp8, q_scale: float, cache, block_table, seq_lens, out, worksp
     """decode() with an e4m3 query ``q_fp8`` [T, N, 576] (quantised with
     q_scale) over an e4m3 cache: fp8 x fp8 score MMAs."""
     T, N, _ = q_fp8.shape
-    nb, ps, _ = cache.shape
+    nb, ps, _ = _decode_checked(None, None, cache, block_table, seq_lens, out, query_start_loc, lse, q8=q_fp8)
+    _dense(workspace, "workspace", (workspace.dtype,))
     B = seq_lens.numel()
     _check(load().mla_decode_fp8q(_ptr(q_fp8), float(q_scale), _ptr(cache), nb, ps, float(kv_scale),
                                   _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
@@ -174,11 +237,36 @@ def decode_status(workspace, stream=None) -> int:
     return st.value
 
 
+def decode_no_alloc_status(clear: bool = False, stream=None) -> int:
+    """Device error word of the last decode_no_alloc on the current device
+    (OR of the DEVERR_* bits); optionally cleared afterwards."""
+    st = ctypes.c_int(0)
+    _check(load().mla_decode_no_alloc_status(ctypes.byref(st), int(clear), _stream(stream)))
+    return st.value
+
+
+def set_decode_wait_test(skip_first_tile: bool = False, wait_limit_ns: int = 0) -> None:
+    """Test aid for the bounded on-chip waits: later decodes of this thread
+    run with every wait bounded by ``wait_limit_ns`` (0: the default 1 s) and,
+    with ``skip_first_tile``, one CTA never loads its first cache tile, so a
+    wait for it runs out and the device error word gets DEVERR_TIMEOUT."""
+    _check(load().mla_set_decode_wait_test(int(bool(skip_first_tile)), int(wait_limit_ns)))
+
+
 def merge_states(o_a, lse_a, o_b, lse_b, out, lse_out=None, stream=None) -> None:
     """merge_attn_states of two partials (rows x dim, bf16 or fp32)."""
     import torch
+    _dense(lse_a, "lse_a", torch.float32, dims=1)
     rows = lse_a.numel()
+    _dense(o_a, "o_a", (torch.bfloat16, torch.float32))
     dim = o_a.numel() // max(rows, 1)
+    if rows > 0 and (o_a.numel() != rows * dim or o_a.shape[0] != rows):
+        raise ValueError(f"o_a must hold one row per LSE entry ({rows}), got shape {tuple(o_a.shape)}")
+    _dense(o_b, "o_b", o_a.dtype, tuple(o_a.shape))
+    _dense(out, "out", o_a.dtype, tuple(o_a.shape))
+    _dense(lse_b, "lse_b", torch.float32, (rows,))
+    if lse_out is not None:
+        _dense(lse_out, "lse_out", torch.float32, (rows,))
     code = MLA_BF16 if o_a.dtype == torch.bfloat16 else MLA_FP32
     _check(load().mla_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), rows, dim, code, _ptr(out),
                                    _ptr(lse_out), _stream(stream)))
@@ -189,16 +277,25 @@ def q_absorb(q_nope, w_uk_t, ql_nope, stream=None) -> None:
     ``q_nope`` [T, N, P] may be a column slice of a wider tensor (for example
     ``q[..., :128]`` of q = [q_nope | q_pe]): its last dimension must be
     contiguous and the (t, n) rows equally spaced."""
+    import torch
     T, N, P_ = q_nope.shape
+    if q_nope.dtype != torch.bfloat16:
+        raise ValueError(f"q_nope must be bfloat16, got {q_nope.dtype}")
     if q_nope.stride(2) != 1 or q_nope.stride(0) != N * q_nope.stride(1):
         raise ValueError("q_nope rows must be equally spaced with a contiguous last dimension")
+    _dense(w_uk_t, "w_uk_t", torch.bfloat16, (N, P_, LKV))
+    _dense(ql_nope, "ql_nope", torch.bfloat16, (T, N, LKV))
     _check(load().mla_q_absorb(_ptr(q_nope), q_nope.stride(1), _ptr(w_uk_t), T, N, P_, _ptr(ql_nope),
                                _stream(stream)))
 
 
 def v_up_proj(o_lat, w_uv, out, stream=None) -> None:
     """out[t, n, :] = o_lat[t, n, :] @ w_uv[n] (bf16; w_uv [N, 512, V], out [T, N, V])."""
+    import torch
+    _dense(o_lat, "o_lat", torch.bfloat16, (None, None, LKV))
     T, N, _ = o_lat.shape
+    _dense(w_uv, "w_uv", torch.bfloat16, (N, LKV, None))
+    _dense(out, "out", torch.bfloat16, (T, N, w_uv.shape[2]))
     _check(load().mla_v_up_proj(_ptr(o_lat), _ptr(w_uv), T, N, w_uv.shape[2], _ptr(out), _stream(stream)))
 
 
@@ -206,10 +303,16 @@ def gather_cache(cache, block_table, cu_seq_lens, dst, seq_starts=None, kv_scale
                  stream=None) -> None:
     """gather_and_maybe_dequant_cache: dst [num_tokens, 576] bf16 receives the
     chunk rows of every request (cu_seq_lens [B+1], seq_starts [B] int32)."""
-    nb, ps, w = cache.shape
-    if w != DQK:
-        raise ValueError(f"cache rows must be {DQK} wide, got {w}")
+    import torch
+    nb, ps, _ = _cache_checked(cache)
+    _dense(cu_seq_lens, "cu_seq_lens", torch.int32, dims=1)
     B = cu_seq_lens.numel() - 1
+    _dense(block_table, "block_table", torch.int32, dims=2)
+    if seq_starts is not None:
+        _dense(seq_starts, "seq_starts", torch.int32, (B,))
+    _dense(dst, "dst", torch.bfloat16, (None, DQK))
+    if status is not None:
+        _dense(status, "status", torch.int32, (1,))
     _check(load().mla_gather_cache(_ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale), _ptr(block_table),
                                    block_table.shape[1], _ptr(cu_seq_lens), _ptr(seq_starts), B, _ptr(dst),
                                    dst.shape[0], _ptr(status), _stream(stream)))
