@@ -1,6 +1,7 @@
 // concat_and_cache_mla: write the latent rows [kv_c | k_pe] of new tokens into
-// the paged cache at their slots (vllm/v1/attention/backends/mla/common.py,
-// MLACommonImpl.forward, "write the latent and rope to kv cache").
+// the paged cache at their slots (page "vllm/v1/attention/backends/mla/
+// common.py", MLACommonImpl.forward: the cache update that precedes the
+// attention of a step).
 //
 // One warp per token.  A bf16 row is 72 16-byte vectors (64 of kv_c, 8 of
 // k_pe) moved with 16-byte loads and stores.  For an e4m3 cache every value is

@@ -57,6 +57,26 @@ int scratch_address(void** out) {
 
 }  // namespace
 
+// Copies (and on request clears) the device error word of the last
+// allocation-free decode on the current device: the first int of the static
+// scratch, where the decode's plan header keeps it.
+extern "C" int mla_decode_no_alloc_status(int* status, int clear, void* stream) {
+  if (!status) return mla::report_error(MLA_ERR_INVALID_ARG, "null pointer argument");
+  void* ws = nullptr;
+  const int rc = scratch_address(&ws);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(status, ws, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "reading the allocation-free decode's error word failed: %s", cudaGetErrorString(e));
+    return mla::report_error(MLA_ERR_CUDA, msg);
+  }
+  return MLA_OK;
+}
+
 extern "C" int mla_decode_no_alloc(const void* q_abs, const void* q_pe, const void* cache, int64_t num_blocks,
                                    int page_size, int cache_dtype, float kv_scale, const int32_t* block_table,
                                    int max_pages_per_seq, const int32_t* seq_lens, int batch,

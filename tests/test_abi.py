@@ -200,3 +200,68 @@ def test_fp8_query_decode_validation_rejects_before_launch(lib):
     assert call(q=None) == -1 and b"null" in lib.mla_last_error()
     assert call(ws_bytes=16) != 0 and b"workspace" in lib.mla_last_error()
     assert call(batch=0, total_q=0) == 0
+
+
+def test_binding_refuses_layouts_the_kernels_would_misread():
+    """The kernels read dense rows of fixed element types; the binding refuses
+    column slices, transposed views and wrong integer widths before any call
+    (host tensors suffice: the checks come before any device address)."""
+    import torch
+    import mla_latent_kv_15_gb300 as mla
+    cache = torch.empty((4, 64, 576), dtype=torch.bfloat16)
+    proj = torch.empty((8, 640), dtype=torch.bfloat16)          # a [T, 576 + 64] projection output
+    kv_c_slice = proj[:, :512]                                  # column slice: rows 640 apart
+    k_pe = torch.empty((8, 64), dtype=torch.bfloat16)
+    slots64 = torch.arange(8, dtype=torch.int64)
+    with pytest.raises(ValueError, match="kv_c must be contiguous"):
+        mla.cache_write(kv_c_slice, k_pe, slots64, cache)
+    with pytest.raises(ValueError, match="slot_mapping must be int64"):
+        mla.cache_write(torch.empty((8, 512), dtype=torch.bfloat16), k_pe, slots64.to(torch.int32), cache)
+    with pytest.raises(ValueError, match="k_pe must have shape"):
+        mla.cache_write(torch.empty((8, 512), dtype=torch.bfloat16), k_pe[:4], slots64, cache)
+    with pytest.raises(ValueError, match="kv_c must be bfloat16"):
+        mla.cache_write(torch.empty((8, 512), dtype=torch.float16), k_pe, slots64, cache)
+
+    T, N, B = 4, 16, 4
+    q_abs = torch.empty((T, N, 512), dtype=torch.bfloat16)
+    q_pe = torch.empty((T, N, 64), dtype=torch.bfloat16)
+    bt = torch.zeros((B, 2), dtype=torch.int32)
+    sl = torch.ones(B, dtype=torch.int32)
+    out = torch.empty((T, N, 512), dtype=torch.bfloat16)
+    ws = torch.empty(1 << 20, dtype=torch.uint8)
+    ok = dict(q_abs=q_abs, q_pe=q_pe, cache=cache, block_table=bt, seq_lens=sl, out=out, workspace=ws)
+
+    def call(**over):
+        kw = dict(ok)
+        kw.update(over)
+        mla.decode(kw["q_abs"], kw["q_pe"], kw["cache"], kw["block_table"], kw["seq_lens"], kw["out"],
+                   kw["workspace"], scale=0.07, lse=kw.get("lse"), query_start_loc=kw.get("qsl"))
+
+    with pytest.raises(ValueError, match="q_abs must be contiguous"):
+        call(q_abs=torch.empty((N, T, 512), dtype=torch.bfloat16).transpose(0, 1))   # a bmm's [N, T, L] output
+    with pytest.raises(ValueError, match="q_pe must have shape"):
+        call(q_pe=torch.empty((T, N, 32), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="block_table must be int32"):
+        call(block_table=bt.to(torch.int64))
+    with pytest.raises(ValueError, match="seq_lens must be int32"):
+        call(seq_lens=sl.to(torch.int64))
+    with pytest.raises(ValueError, match="query_start_loc must have shape"):
+        call(qsl=torch.zeros(B, dtype=torch.int32))
+    with pytest.raises(ValueError, match="out must be bfloat16"):
+        call(out=torch.empty((T, N, 512), dtype=torch.float32))
+    with pytest.raises(ValueError, match="lse must be float32"):
+        call(lse=torch.empty((T, N), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="cache rows must be 576"):
+        call(cache=torch.empty((4, 64, 512), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="cache must be"):
+        call(cache=torch.empty((4, 64, 576), dtype=torch.float32))
+    # a well-formed call gets past every check (and then needs the device)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        call()
+    # merge: mismatched partner shapes and LSE dtype
+    o = torch.empty((10, 512), dtype=torch.float32)
+    l32 = torch.empty(10, dtype=torch.float32)
+    with pytest.raises(ValueError, match="o_b must have shape"):
+        mla.merge_states(o, l32, torch.empty((10, 256), dtype=torch.float32), l32, o)
+    with pytest.raises(ValueError, match="lse_b must be float32"):
+        mla.merge_states(o, l32, o, l32.double(), o)

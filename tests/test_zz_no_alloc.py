@@ -59,3 +59,22 @@ def test_no_alloc_rejects_batches_beyond_its_scratch():
     rc = lib.mla_decode_no_alloc(fake, fake, fake, 100, 64, 0, 1.0, fake, 8, fake, batch, fake, total_q, heads,
                                  0.07, 0, fake, None, None)
     assert rc == -4 and b"static scratch" in lib.mla_last_error()
+
+
+@pytest.mark.gpu
+def test_no_alloc_status_reports_bad_block_ids():
+    """Callers without a workspace read the device error word through
+    mla_decode_no_alloc_status: a block-table entry past the cache sets
+    MLA_DEVERR_BAD_BLOCK, a clean call leaves 0."""
+    case = synth.make_decode_case(num_heads=16, batch=3, ctx=(100, 300), page_size=64, seed=79, poison=False)
+    g = GpuCase(case)
+    out = torch.empty_like(g.out)
+    lse = torch.empty_like(g.lse)
+    _no_alloc(g, out, lse)
+    assert mla.decode_no_alloc_status() == 0
+    bad = g.block_table.clone()
+    bad[1, 0] = case.num_blocks + 3
+    g.block_table = bad
+    _no_alloc(g, out, lse)
+    assert mla.decode_no_alloc_status(clear=True) & mla.DEVERR_BAD_BLOCK
+    assert mla.decode_no_alloc_status() == 0                 # cleared
