@@ -269,8 +269,7 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-// Maximum and minimum of 64 values (NaN entries are ignored: max/min return
-// the other operand).
+// Maximum of 64 values (NaN entries are ignored: max returns the other operand).
 __device__ __forceinline__ float max64(const float (&x)[kTile]) {
   float m[22];
 #pragma unroll
@@ -281,31 +280,27 @@ __device__ __forceinline__ float max64(const float (&x)[kTile]) {
   m[7] = m[21];
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
-__device__ __forceinline__ float min64(const float (&x)[kTile]) {
-  float m[22];
-#pragma unroll
-  for (int c = 0; c < 21; ++c) m[c] = fmin3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
-  m[21] = x[63];
-#pragma unroll
-  for (int c = 0; c < 7; ++c) m[c] = fmin3(m[3 * c], m[3 * c + 1], m[3 * c + 2]);
-  m[7] = m[21];
-  return fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])));
-}
 
-// Maximum and minimum over the first n of 64 values (n >= 64: all), the
-// others left out; both NaN if n <= 0.
-__device__ __forceinline__ void range64(const float (&x)[kTile], int n, float& hi, float& lo) {
-  if (n >= kTile) {
-    hi = max64(x);
-    lo = min64(x);
-    return;
-  }
+// Maximum and minimum over the first n of the 64 values (n < 64: a row's
+// last, ragged tile; the other values are left out); NaN if n <= 0.
+__device__ __forceinline__ void range_first_n(const float (&x)[kTile], int n, float& hi, float& lo) {
   const float nan = __int_as_float(0x7fffffff);
-  float y[kTile];
+  float h[22], l[22];
 #pragma unroll
-  for (int c = 0; c < kTile; ++c) y[c] = c < n ? x[c] : nan;
-  hi = max64(y);
-  lo = min64(y);
+  for (int c = 0; c < 21; ++c) {
+    const float a = 3 * c < n ? x[3 * c] : nan, b = 3 * c + 1 < n ? x[3 * c + 1] : nan,
+                d = 3 * c + 2 < n ? x[3 * c + 2] : nan;
+    h[c] = fmax3(a, b, d);
+    l[c] = fmin3(a, b, d);
+  }
+  h[21] = l[21] = 63 < n ? x[63] : nan;
+#pragma unroll
+  for (int c = 0; c < 7; ++c) {
+    h[c] = fmax3(h[3 * c], h[3 * c + 1], h[3 * c + 2]);
+    l[c] = fmin3(l[3 * c], l[3 * c + 1], l[3 * c + 2]);
+  }
+  hi = fmaxf(fmax3(h[0], h[1], h[2]), fmax3(h[3], h[4], fmax3(h[5], h[6], h[21])));
+  lo = fminf(fmin3(l[0], l[1], l[2]), fmin3(l[3], l[4], fmin3(l[5], l[6], l[21])));
 }
 
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint32_t (&o)[8]) {
@@ -703,24 +698,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // 32-byte stores allowed
     int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
-    // Load partial scores of tile `t` from TMEM into `dst` and free the S columns.
-    auto load_s = [&](uint32_t t, float (&dst)[kTile]) {
+    // Load partial scores of tile `t` from TMEM into `dst` and free the S
+    // columns; `hi` and `lo` get the row's largest and smallest partial (the
+    // reducing TMEM loads of sm_103a compute them on the way).
+    auto load_s = [&](uint32_t t, float (&dst)[kTile], float& hi, float& lo) {
       wait_bar(ctx, &bars->s_full, t & 1);
       __syncwarp();
       tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tl + kTmemS, r0);
-      tmem_ld32(tl + kTmemS + 32, r1);
+      uint32_t r[kTile];
+      tmem_ld64_max(tl + kTmemS, r, hi);
+      tmem_ld64_min(tl + kTmemS, r, lo);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        dst[c] = __uint_as_float(r0[c]);
-        dst[32 + c] = __uint_as_float(r1[c]);
-      }
+      for (int c = 0; c < kTile; ++c) dst[c] = __uint_as_float(r[c]);
       if constexpr (kQ8) {
         // sums of code products -> real partial scores (both halves in the same units)
 #pragma unroll
         for (int c = 0; c < kTile; ++c) dst[c] *= a.qk_scale;
+        hi *= a.qk_scale;
+        lo *= a.qk_scale;
       }
       tc_fence_before();
       __syncwarp();
@@ -728,21 +724,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     };
     // Send partial scores of tile `t` (valid rows only) straight into the
     // peer's receive buffer as 16-bit block fixed point: codes of (s - c) /
-    // step over the keys the row may see (`nvis` of the tile's 64), then the
-    // row header (c, step).  16-byte st.async stores that count against the
-    // peer's barrier (this keeps the exchange off the TMA engine that streams
-    // the cache tiles).
-    auto send_s = [&](uint32_t t, const float (&src)[kTile], int nvis) {
+    // step over the `nvis` keys of the tile the row may see, c the middle of
+    // their range [lo, hi] and step = half the range / 32766 (the range of a
+    // full tile comes from the loads, a ragged tile's is recomputed over its
+    // visible keys), then the row header (c, step).  16-byte st.async stores
+    // that count against the peer's barrier (this keeps the exchange off the
+    // TMA engine that streams the cache tiles).
+    auto send_s = [&](uint32_t t, const float (&src)[kTile], int nvis, float hi, float lo) {
       const uint32_t b = t % kXBuffers;
       if (row < nrows_cur) {
-        float hi, lo;
-        range64(src, nvis, hi, lo);
+        if (nvis < kTile) range_first_n(src, nvis, hi, lo);
         if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this tile
         const float ctr = 0.5f * (hi + lo);
-        // |fl(s - ctr)| <= half for every s in [lo, hi] (monotone rounding)
         const float half = fmaxf(fmaxf(hi - ctr, ctr - lo), 1e-30f);
         const float step = half * (1.f / kCodeRange);
         const float inv = __fdividef(kCodeRange, half);
+        // code + 32768 = s * inv + (magic - c * inv), rounded to an integer by
+        // the FMA (within 1.5 steps of the exact code)
+        const float off = kCodeMagic - ctr * inv;
         const uint32_t base = xrecv_peer0 + b * kXBytes + xrow;
         const uint32_t bar = xfull_peer0 + b * 8;
 #pragma unroll
@@ -750,10 +749,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           uint32_t w[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            float d0 = src[8 * c + 2 * j], d1 = src[8 * c + 2 * j + 1];
-            add2(d0, d1, -ctr, -ctr);
             float f0, f1;
-            fma2(f0, f1, d0, d1, inv, kCodeMagic);      // rounds to the integer code + 32768
+            fma2(f0, f1, src[8 * c + 2 * j], src[8 * c + 2 * j + 1], inv, off);
             w[j] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
           }
           st_async_v4(base + c * kXChunk, w[0], w[1], w[2], w[3], bar);
@@ -912,14 +909,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       auto nvis = [&](int jj) { return Lr - (ur.tile_begin + jj) * kTile; };
       float cur[kTile], nxt[kTile];
       if (ntiles > 0) {
-        load_s(it, cur);
-        send_s(it, cur, nvis(0));
+        float hi, lo;
+        load_s(it, cur, hi, lo);
+        send_s(it, cur, nvis(0), hi, lo);
       }
       for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
         // exchange of the next tile first: the network copy overlaps this tile's work
         if (jj + 1 < ntiles) {
-          load_s(it + 1, nxt);
-          send_s(it + 1, nxt, nvis(jj + 1));
+          float hi, lo;
+          load_s(it + 1, nxt, hi, lo);
+          send_s(it + 1, nxt, nvis(jj + 1), hi, lo);
         }
         const float cpeer = recv_s(it, cur, nbytes);   // cur = own + peer partial - cpeer
 

@@ -342,6 +342,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 32 lanes x 32-bit, 64 consecutive columns, with the thread's maximum
+// (tmem_ld64_max) or minimum (tmem_ld64_min) of its 64 loaded values as an
+// extra result; the reduction ignores NaN values (sm_103a).
+#define MLA_R64(i) "=r"(r[i])
+#define MLA_TMEM_LD64_RED(NAME, OP)                                                                                    \
+  __device__ __forceinline__ void NAME(uint32_t taddr, uint32_t(&r)[64], float& red) {                                 \
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x64." OP                                                          \
+                 ".f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "   \
+                 "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, "     \
+                 "%39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "     \
+                 "%58, %59, %60, %61, %62, %63}, %64, [%65];"                                                          \
+                 : MLA_R64(0), MLA_R64(1), MLA_R64(2), MLA_R64(3), MLA_R64(4), MLA_R64(5), MLA_R64(6), MLA_R64(7),    \
+                   MLA_R64(8), MLA_R64(9), MLA_R64(10), MLA_R64(11), MLA_R64(12), MLA_R64(13), MLA_R64(14),            \
+                   MLA_R64(15), MLA_R64(16), MLA_R64(17), MLA_R64(18), MLA_R64(19), MLA_R64(20), MLA_R64(21),          \
+                   MLA_R64(22), MLA_R64(23), MLA_R64(24), MLA_R64(25), MLA_R64(26), MLA_R64(27), MLA_R64(28),          \
+                   MLA_R64(29), MLA_R64(30), MLA_R64(31), MLA_R64(32), MLA_R64(33), MLA_R64(34), MLA_R64(35),          \
+                   MLA_R64(36), MLA_R64(37), MLA_R64(38), MLA_R64(39), MLA_R64(40), MLA_R64(41), MLA_R64(42),          \
+                   MLA_R64(43), MLA_R64(44), MLA_R64(45), MLA_R64(46), MLA_R64(47), MLA_R64(48), MLA_R64(49),          \
+                   MLA_R64(50), MLA_R64(51), MLA_R64(52), MLA_R64(53), MLA_R64(54), MLA_R64(55), MLA_R64(56),          \
+                   MLA_R64(57), MLA_R64(58), MLA_R64(59), MLA_R64(60), MLA_R64(61), MLA_R64(62), MLA_R64(63),          \
+                   "=f"(red)                                                                                           \
+                 : "r"(taddr)                                                                                          \
+                 : "memory");                                                                                          \
+  }
+MLA_TMEM_LD64_RED(tmem_ld64_max, "max")
+MLA_TMEM_LD64_RED(tmem_ld64_min, "min")
+#undef MLA_TMEM_LD64_RED
+#undef MLA_R64
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
