@@ -106,29 +106,25 @@ struct Layout {
   static constexpr int kXRows = kVariant == 2 ? 32 : kRows;        // rows of a receive buffer
   static constexpr int kXChunk = kXRows * 16;                      // one 16-byte chunk of every row
   static constexpr int kXHdr = 8 * kXChunk;                        // row headers after the 8 code chunks
-  static constexpr int kXBytes = kXHdr + kXRows * 8;               // codes + (centre, step) per row
+  static constexpr int kXBytes = kXHdr + kXRows * 16;              // codes + (centre, step) per row half
 };
 constexpr int kXBuffers = 4;                      // receive ring (4: reuse needs no handshake)
-constexpr uint32_t kXRowBytes = kTile * 2 + 8;    // exchanged bytes per row and tile
-// Warp roles.
-//  bf16 cache (224 threads): 0 TMA producer, 1 score-MMA issuer (and TMEM
-//    owner), 2 P.V-MMA issuer, 3-6 softmax.
-//  e4m3 cache (384 threads, grouped by warpgroup so that each group gets its
-//    own register budget): 0-3 softmax, 4-7 e4m3 expansion, 8 TMA producer,
-//    9 score-MMA issuer, 10 P.V-MMA issuer, 11 idle.
-template <int kCacheFp8>
+constexpr uint32_t kXRowBytes = 2 * (kTile + 8);  // exchanged bytes per row and tile: two halves, codes + header
+// Warp roles.  Warps 0-7: softmax / exchange / O rescale / epilogue, two
+// threads per query row (warp w: TMEM lanes 32(w%4).., key half and output
+// half w/4).  Warp 8: TMA producer; 9: score-MMA issuer (and TMEM owner);
+// 10: P.V-MMA issuer; 11 idle; e4m3 cache: 12-15 expand e4m3 tiles to bf16.
+template <int kVariant>
 struct Roles {
-  static constexpr int kThreads = kCacheFp8 ? 384 : 224;
-  static constexpr int kSoftmax0 = kCacheFp8 ? 0 : 3;
-  static constexpr int kProducer = kCacheFp8 ? 8 : 0;
-  static constexpr int kScore = kCacheFp8 ? 9 : 1;
-  static constexpr int kPV = kCacheFp8 ? 10 : 2;
+  static constexpr int kThreads = (kVariant == 1 || kVariant == 3) ? 512 : 384;
 };
-constexpr int kWarpExpand0 = 4;   // e4m3 cache only
-// e4m3 registers per thread after the split (launch: 168): 128 x (248 + 120 +
-// 112) = 61440 stay within the 384 x 168 the CTA is launched with.
-constexpr uint32_t kRegsSoftmax = 248, kRegsExpand = 120, kRegsIssue = 112;
-static_assert(128 * (kRegsSoftmax + kRegsExpand + kRegsIssue) <= 384 * 168, "register split");
+constexpr int kSoftmaxWarps = 8;
+// e4m3 cache: register budget per thread of each warpgroup (two softmax
+// groups, the producer/issuer group, the expansion group) within the 512 x 128
+// the CTA is launched with
+constexpr uint32_t kRegsSoftmax8 = 160, kRegsIssue8 = 96, kRegsExpand8 = 96;
+static_assert(128 * (2 * kRegsSoftmax8 + kRegsIssue8 + kRegsExpand8) <= 512 * 128, "register split");
+constexpr int kWarpProducer = 8, kWarpScore = 9, kWarpPV = 10, kWarpExpand0 = 12;
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
 
 constexpr uint32_t kTmemO = 0;
@@ -164,10 +160,14 @@ struct __align__(8) Barriers {
   int abort;
 };
 
+// the two threads of a row exchange their tile maxima (two parities) and,
+// at the end of a unit, their row sums: [2][2][128] + [2][128] floats
+constexpr int kPairFloats = 2 * 2 * kRows + 2 * kRows;
+
 template <int kVariant>
 constexpr size_t smem_bytes() {
   return 1024 + (size_t)Layout<kVariant>::kStages * kStageBytes +
-         kXBuffers * (size_t)Layout<kVariant>::kXBytes + sizeof(Barriers);
+         kXBuffers * (size_t)Layout<kVariant>::kXBytes + sizeof(Barriers) + 16 + kPairFloats * sizeof(float);
 }
 static_assert(smem_bytes<0>() <= 232448 && smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
                   smem_bytes<3>() <= 232448,
@@ -203,7 +203,9 @@ __device__ __forceinline__ void wait_bar_cluster(const Ctx& c, uint64_t* bar, ui
   if (!mbar_wait_cluster(smem_u32(bar), parity, lim)) raise_error(c, 1);
 }
 
-__device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void named_bar_softmax() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// the two warps holding the halves of the same rows (warps q and q + 4)
+__device__ __forceinline__ void named_bar_pair(int q) { asm volatile("bar.sync %0, 64;" ::"r"(3 + q) : "memory"); }
 __device__ __forceinline__ void named_bar_expand() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -281,26 +283,23 @@ __device__ __forceinline__ float max64(const float (&x)[kTile]) {
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
-// Maximum and minimum over the first n of the 64 values (n < 64: a row's
-// last, ragged tile; the other values are left out); NaN if n <= 0.
-__device__ __forceinline__ void range_first_n(const float (&x)[kTile], int n, float& hi, float& lo) {
+// Maximum and minimum over the first n of 32 values (n < 32: the last,
+// ragged tile of a row; the other values are left out); NaN if n <= 0.
+__device__ __forceinline__ void range_first_n(const float (&x)[kTile / 2], int n, float& hi, float& lo) {
   const float nan = __int_as_float(0x7fffffff);
-  float h[22], l[22];
+  float h[11], l[11];
 #pragma unroll
-  for (int c = 0; c < 21; ++c) {
+  for (int c = 0; c < 10; ++c) {
     const float a = 3 * c < n ? x[3 * c] : nan, b = 3 * c + 1 < n ? x[3 * c + 1] : nan,
                 d = 3 * c + 2 < n ? x[3 * c + 2] : nan;
     h[c] = fmax3(a, b, d);
     l[c] = fmin3(a, b, d);
   }
-  h[21] = l[21] = 63 < n ? x[63] : nan;
-#pragma unroll
-  for (int c = 0; c < 7; ++c) {
-    h[c] = fmax3(h[3 * c], h[3 * c + 1], h[3 * c + 2]);
-    l[c] = fmin3(l[3 * c], l[3 * c + 1], l[3 * c + 2]);
-  }
-  hi = fmaxf(fmax3(h[0], h[1], h[2]), fmax3(h[3], h[4], fmax3(h[5], h[6], h[21])));
-  lo = fminf(fmin3(l[0], l[1], l[2]), fmin3(l[3], l[4], fmin3(l[5], l[6], l[21])));
+  const float a = 30 < n ? x[30] : nan, b = 31 < n ? x[31] : nan;
+  h[10] = fmaxf(a, b);
+  l[10] = fminf(a, b);
+  hi = fmax3(fmax3(h[0], h[1], h[2]), fmax3(h[3], h[4], h[5]), fmax3(h[6], h[7], fmax3(h[8], h[9], h[10])));
+  lo = fmin3(fmin3(l[0], l[1], l[2]), fmin3(l[3], l[4], l[5]), fmin3(l[6], l[7], fmin3(l[8], l[9], l[10])));
 }
 
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 v, uint32_t (&o)[8]) {
@@ -358,7 +357,7 @@ __device__ __forceinline__ void expand_e4m3_tile(uint32_t stage, int t) {
 }
 
 template <int kVariant>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 || kVariant == 3>::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
                   const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kvr,
                   const DecodeArgs a) {
@@ -372,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   uint8_t* stages = smem;
   uint8_t* x_recv = stages + kStages * kStageBytes;      // receive ring
   Barriers* bars = reinterpret_cast<Barriers*>(x_recv + kXBuffers * kXBytes);
+  float* pairbuf = reinterpret_cast<float*>(((uintptr_t)(bars + 1) + 15) & ~(uintptr_t)15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -389,8 +389,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     for (int i = 0; i < kMaxStages; ++i) mbar_init(smem_u32(&bars->kx_free[i]), 1);
     mbar_init(smem_u32(&bars->q_ready), 1);
     mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->s_free), 4);
-    mbar_init(smem_u32(&bars->p_full), 4);
+    mbar_init(smem_u32(&bars->s_free), kSoftmaxWarps);
+    mbar_init(smem_u32(&bars->p_full), kSoftmaxWarps);
     mbar_init(smem_u32(&bars->p_free), 1);
     mbar_init(smem_u32(&bars->o_full), 1);
     for (int i = 0; i < kXBuffers; ++i) mbar_init(smem_u32(&bars->x_full[i]), 1);
@@ -399,12 +399,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
     bars->abort = 0;
     fence_mbar_init();
   }
-  using R = Roles<kCacheFp8>;
-  if (warp == R::kScore) {
+  if (warp == kWarpScore) {
     tmem_alloc(smem_u32(&bars->tmem_base), 512);
     tmem_relinquish();
   }
-  if (warp == R::kProducer && lane == 0) {
+  if (warp == kWarpProducer && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_qr);
     tma_prefetch_desc(&tm_kv);
@@ -633,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   };
   auto expander = [&]() {
     // -------------------------------------------------------- e4m3 expansion
-    const int te = threadIdx.x - 32 * kWarpExpand0;
+    const int te = threadIdx.x - 32 * kWarpExpand0;   // 0..127
     uint32_t item = 0;
     for (int u = ubeg; u < uend; ++u) {
       const UnitRec ur = P.units[u];
@@ -682,39 +681,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
   };
   auto softmax = [&]() {
     // ------------------------------------- softmax / exchange / rescale / epilogue
+    // Two threads per query row: warp w handles TMEM lanes 32(w%4).. (the
+    // rows), keys [32h, 32h+32) of every tile and O columns [128h, 128h+128)
+    // with h = w / 4.  Both halves of a row keep the same running maximum:
+    // they exchange their tile maxima through shared memory every tile.
+    constexpr int kHalf = kTile / 2;         // keys of a tile per thread
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
+    const int hh = warp >> 2;                // key half / output half
     const int row = q4 * 32 + lane;          // query row of this thread in the unit
     const uint32_t tl = tbase + ((uint32_t)(q4 * 32) << 16);
-    const int tid128 = threadIdx.x - 32 * R::kSoftmax0;
-    // receive buffers are chunk-major, [8][kXRows][16 B]: the 32 lanes of a
-    // warp write (and read) 512 contiguous bytes per instruction
-    const uint32_t xrow = (uint32_t)row * 16;
+    const int tid = threadIdx.x;             // 0..255
+    // receive buffers: codes chunk-major, [8][kXRows][16 B] (chunk c = keys
+    // 8c..8c+7, so half h owns chunks 4h..4h+3; the 32 lanes of a warp write
+    // and read 512 contiguous bytes per instruction), then the headers
+    // [2][kXRows][8 B]
     constexpr uint32_t kXChunk = (uint32_t)Layout<kVariant>::kXChunk;
     constexpr uint32_t kXHdr = (uint32_t)Layout<kVariant>::kXHdr;
+    const uint32_t xcode = (uint32_t)row * 16 + 4 * (uint32_t)hh * kXChunk;
+    const uint32_t xhdr = kXHdr + (uint32_t)(hh * kXRows + row) * 8;
     const uint32_t xrecv0 = smem_u32(x_recv);
     const uint32_t xrecv_peer0 = mapa(xrecv0, peer);
     const uint32_t xfull_peer0 = mapa(smem_u32(&bars->x_full[0]), peer);
+    float* pmax = pairbuf;                   // [parity][half][row]
+    float* psum = pairbuf + 4 * kRows;       // [half][row]
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // 32-byte stores allowed
     int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
-    // Load partial scores of tile `t` from TMEM into `dst` and free the S
-    // columns; `hi` and `lo` get the row's largest and smallest partial (the
-    // reducing TMEM loads of sm_103a compute them on the way).
-    auto load_s = [&](uint32_t t, float (&dst)[kTile], float& hi, float& lo) {
+    // Load this half's partial scores of tile `t` from TMEM into `dst` and
+    // free the S columns; `hi` and `lo` get their largest and smallest value
+    // (the reducing TMEM loads of sm_103a compute them on the way).
+    auto load_s = [&](uint32_t t, float (&dst)[kHalf], float& hi, float& lo) {
       wait_bar(ctx, &bars->s_full, t & 1);
       __syncwarp();
       tc_fence_after();
-      uint32_t r[kTile];
-      tmem_ld64_max(tl + kTmemS, r, hi);
-      tmem_ld64_min(tl + kTmemS, r, lo);
+      uint32_t r[kHalf];
+      tmem_ld32_max(tl + kTmemS + kHalf * hh, r, hi);
+      tmem_ld32_min(tl + kTmemS + kHalf * hh, r, lo);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) dst[c] = __uint_as_float(r[c]);
+      for (int c = 0; c < kHalf; ++c) dst[c] = __uint_as_float(r[c]);
       if constexpr (kQ8) {
         // sums of code products -> real partial scores (both halves in the same units)
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) dst[c] *= a.qk_scale;
+        for (int c = 0; c < kHalf; ++c) dst[c] *= a.qk_scale;
         hi *= a.qk_scale;
         lo *= a.qk_scale;
       }
@@ -722,19 +732,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->s_free));
     };
-    // Send partial scores of tile `t` (valid rows only) straight into the
-    // peer's receive buffer as 16-bit block fixed point: codes of (s - c) /
-    // step over the `nvis` keys of the tile the row may see, c the middle of
-    // their range [lo, hi] and step = half the range / 32766 (the range of a
-    // full tile comes from the loads, a ragged tile's is recomputed over its
-    // visible keys), then the row header (c, step).  16-byte st.async stores
-    // that count against the peer's barrier (this keeps the exchange off the
-    // TMA engine that streams the cache tiles).
-    auto send_s = [&](uint32_t t, const float (&src)[kTile], int nvis, float hi, float lo) {
+    // Send this half's partial scores of tile `t` (valid rows only) straight
+    // into the peer's receive buffer as 16-bit block fixed point: codes of
+    // (s - c) / step over the `nvis` of its 32 keys the row may see, c the
+    // middle of their range [lo, hi] and step = half the range / 32766 (the
+    // range of a full half comes from the loads, a ragged one's is recomputed
+    // over its visible keys), then the header (c, step) of the half.  16-byte
+    // st.async stores that count against the peer's barrier (this keeps the
+    // exchange off the TMA engine that streams the cache tiles).
+    auto send_s = [&](uint32_t t, const float (&src)[kHalf], int nvis, float hi, float lo) {
       const uint32_t b = t % kXBuffers;
       if (row < nrows_cur) {
-        if (nvis < kTile) range_first_n(src, nvis, hi, lo);
-        if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this tile
+        if (nvis < kHalf) range_first_n(src, nvis, hi, lo);
+        if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this half
         const float ctr = 0.5f * (hi + lo);
         const float half = fmaxf(fmaxf(hi - ctr, ctr - lo), 1e-30f);
         const float step = half * (1.f / kCodeRange);
@@ -742,10 +752,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         // code + 32768 = s * inv + (magic - c * inv), rounded to an integer by
         // the FMA (within 1.5 steps of the exact code)
         const float off = kCodeMagic - ctr * inv;
-        const uint32_t base = xrecv_peer0 + b * kXBytes + xrow;
+        const uint32_t base = xrecv_peer0 + b * kXBytes + xcode;
         const uint32_t bar = xfull_peer0 + b * 8;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kHalf / 8; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -755,25 +765,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           }
           st_async_v4(base + c * kXChunk, w[0], w[1], w[2], w[3], bar);
         }
-        st_async_v2(xrecv_peer0 + b * kXBytes + kXHdr + (uint32_t)row * 8, __float_as_uint(ctr),
-                    __float_as_uint(step), bar);
+        st_async_v2(xrecv_peer0 + b * kXBytes + xhdr, __float_as_uint(ctr), __float_as_uint(step), bar);
       }
     };
-    // Add the peer's partial scores of tile `t`, less the row's centre c, into
-    // `acc`; returns c (the caller folds it into the maximum and the exponent).
-    auto recv_s = [&](uint32_t t, float (&acc)[kTile], uint32_t nbytes) -> float {
+    // Add the peer's partial scores of this half of tile `t`, less the
+    // half's centre c, into `acc`; returns c (the caller folds it into the
+    // maximum and the exponent).
+    auto recv_s = [&](uint32_t t, float (&acc)[kHalf], uint32_t nbytes) -> float {
       const uint32_t b = t % kXBuffers, use = t / kXBuffers;
-      if (tid128 == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
+      if (tid == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
       wait_bar_cluster(ctx, &bars->x_full[b], use & 1);
       __syncwarp();
       float ctr = 0.f;
       if (row < kXRows) {
-        const uint2 h = lds64(xrecv0 + b * kXBytes + kXHdr + (uint32_t)row * 8);
+        const uint2 h = lds64(xrecv0 + b * kXBytes + xhdr);
         ctr = __uint_as_float(h.x);
         const float step = __uint_as_float(h.y);
-        const uint32_t base = xrecv0 + b * kXBytes + xrow;
+        const uint32_t base = xrecv0 + b * kXBytes + xcode;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < kHalf / 8; ++c) {
           const uint4 v = lds128(base + c * kXChunk);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -790,6 +800,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       // buffer three tiles back, whatever the row counts of the units
       named_bar_softmax();
       return ctr;
+    };
+    // Maximum of the two halves' values of a row (pair exchange through
+    // shared memory; the parity alternates so that a write never meets a
+    // read of the previous exchange).
+    auto pair_max = [&](float v, uint32_t parity) {
+      float* pm = pmax + parity * 2 * kRows;
+      pm[hh * kRows + row] = v;
+      named_bar_pair(q4);
+      return fmaxf(v, pm[(1 - hh) * kRows + row]);
     };
 
     uint32_t item = 0, it = 0, units_done = 0;
@@ -814,28 +833,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       const int lmin_warp = __reduce_min_sync(0xffffffffu, Lr);
       const uint32_t nbytes = (uint32_t)gr.nrows * kXRowBytes;
 
-      // the CTA's 288 query dims -> TMEM (A operand of the score MMAs)
+      // the CTA's 288 query dims -> TMEM (A operand of the score MMAs); the
+      // two halves of a row write different columns
+      const uint32_t my = item + (row >= 64 ? 1 : 0);
+      const int k = row & 63;
+      const uint32_t sbase = smem_u32(stages + (my % kStages) * kStageBytes);
       if constexpr (kQ8) {
         // e4m3 query: the nine 32-dim K steps of the CTA's 288 dims (eight
         // from its two 128-dim latent boxes, one from its 32-dim rope box),
-        // four codes per TMEM column, in the order the score issuer walks them
-        const uint32_t my = item + (row >= 64 ? 1 : 0);
+        // four codes per TMEM column, in the order the score issuer walks
+        // them; half h writes latent box h (and h = 1 the rope box)
         wait_bar(ctx, &bars->stg_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
-        const int k = row & 63;
-        const uint32_t base = smem_u32(stages + (my % kStages) * kStageBytes) + kQ8InPlace;
+        const uint32_t base = sbase + kQ8InPlace;
         const uint32_t sgn = a.neg_q ? 0x80808080u : 0u;   // a negative scale negates q
 #pragma unroll
-        for (int p = 0; p < 2; ++p)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint4 v0 = lds128(base + p * kQ8Box + k * 128 + (((2 * kk) ^ (k & 7)) << 4));
-            const uint4 v1 = lds128(base + p * kQ8Box + k * 128 + (((2 * kk + 1) ^ (k & 7)) << 4));
-            const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
-                                   v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
-            tmem_st8(tl + kTmemQ + 32 * p + 8 * kk, w);
-          }
-        {
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 v0 = lds128(base + hh * kQ8Box + k * 128 + (((2 * kk) ^ (k & 7)) << 4));
+          const uint4 v1 = lds128(base + hh * kQ8Box + k * 128 + (((2 * kk + 1) ^ (k & 7)) << 4));
+          const uint32_t w[8] = {v0.x ^ sgn, v0.y ^ sgn, v0.z ^ sgn, v0.w ^ sgn,
+                                 v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
+          tmem_st8(tl + kTmemQ + 32 * hh + 8 * kk, w);
+        }
+        if (hh == 1) {
           // rope box: 32-byte rows, 32-B swizzle (16-byte chunk c of row k at c ^ ((k >> 2) & 1))
           const uint32_t rb = base + 2 * kQ8Box + k * 32;
           const int sw = (k >> 2) & 1;
@@ -845,26 +865,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
                                  v1.x ^ sgn, v1.y ^ sgn, v1.z ^ sgn, v1.w ^ sgn};
           tmem_st8(tl + kTmemQ + 64, w);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_softmax();
-        if (tid128 == 0) {
-          for (int qi = 0; qi < 2; ++qi) {      // two arrivals: the slot's count covers both issuers
-            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
-            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
-          }
-          mbar_arrive(smem_u32(&bars->q_ready));
-        }
-        item += 2;
       } else {
-        const uint32_t my = item + (row >= 64 ? 1 : 0);
+        // bf16 query: half h writes latent boxes 2h, 2h+1 (and h = 1 the q_pe half)
         wait_bar(ctx, &bars->kv_full[my % kStages], (my / kStages) & 1);
         __syncwarp();
-        const int k = row & 63;
-        const uint32_t sbase = smem_u32(stages + (my % kStages) * kStageBytes);
         const uint32_t sgn = a.neg_q ? 0x80008000u : 0u;   // a negative scale negates q
 #pragma unroll
-        for (int p = 0; p < kVBoxes; ++p) {
+        for (int pp = 0; pp < 2; ++pp) {
+          const int p = 2 * hh + pp;
           uint32_t q[32];
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
@@ -876,7 +884,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           }
           tmem_st32(tl + kTmemQ + p * 32, q);
         }
-        {
+        if (hh == 1) {
           // q_pe half: 64-byte rows, 64-B swizzle (chunk c of row k at c ^ ((k >> 1) & 3))
           uint32_t h[16];
           const int sw = (k >> 1) & 3;
@@ -890,24 +898,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           }
           tmem_st16(tl + kTmemQ + 128, h);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        named_bar_softmax();
-        if (tid128 == 0) {
-          for (int qi = 0; qi < 2; ++qi) {      // two arrivals: the slot's count covers both issuers
-            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
-            mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
-          }
-          mbar_arrive(smem_u32(&bars->q_ready));
-        }
-        item += 2;
       }
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_softmax();
+      if (tid == 0) {
+        for (int qi = 0; qi < 2; ++qi) {      // two arrivals: the slot's count covers both issuers
+          mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+          mbar_arrive(smem_u32(&bars->kv_empty[(item + qi) % kStages]));
+        }
+        mbar_arrive(smem_u32(&bars->q_ready));
+      }
+      item += 2;
 
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;          // l: this half's share of the row sum
       const int ntiles = ur.tile_end - ur.tile_begin;
-      // keys of tile jj the row may see (64 on every tile before its last)
-      auto nvis = [&](int jj) { return Lr - (ur.tile_begin + jj) * kTile; };
-      float cur[kTile], nxt[kTile];
+      // keys of this half of tile jj the row may see (32 on every tile before its last)
+      auto nvis = [&](int jj) { return Lr - (ur.tile_begin + jj) * kTile - kHalf * hh; };
+      float cur[kHalf], nxt[kHalf];
       if (ntiles > 0) {
         float hi, lo;
         load_s(it, cur, hi, lo);
@@ -922,14 +930,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         }
         const float cpeer = recv_s(it, cur, nbytes);   // cur = own + peer partial - cpeer
 
-        // mask on ragged tiles, tree max of the unscaled scores (the scale is
-        // positive), then exp2(scale * s - m) as one FMA into the exponential
-        const int key0 = (ur.tile_begin + jj) * kTile;
-        if (key0 + kTile > lmin_warp) {
+        // mask on ragged tiles, max of the unscaled scores of both halves
+        // (the scale is positive), then exp2(scale * s - m) as one FMA
+        const int key0 = (ur.tile_begin + jj) * kTile + kHalf * hh;
+        if (key0 + kHalf > lmin_warp) {
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
+          for (int c = 0; c < kHalf; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
         }
-        const float tmax = (max64(cur) + cpeer) * a.scale_log2;
+        float mx[11];
+#pragma unroll
+        for (int c = 0; c < 10; ++c) mx[c] = fmax3(cur[3 * c], cur[3 * c + 1], cur[3 * c + 2]);
+        mx[10] = fmaxf(cur[30], cur[31]);
+        const float hmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmax3(mx[6], mx[7], fmax3(mx[8], mx[9], mx[10])));
+        const float tmax = pair_max((hmax + cpeer) * a.scale_log2, it & 1);
         float alpha = 1.f;
         if (valid && tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
@@ -937,11 +951,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
           m = tmax;
         }
         const float mref = m == -INFINITY ? 0.f : m;
-        const float kexp = fmaf(cpeer, a.scale_log2, -mref);   // exponent offset of the row
-        uint32_t pk[kTile / 2];
+        const float kexp = fmaf(cpeer, a.scale_log2, -mref);   // exponent offset of this half
+        uint32_t pk[kHalf / 2];
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < kTile / 2; ++c) {
+        for (int c = 0; c < kHalf / 2; ++c) {
           float x0, x1;
           fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, kexp);
           const float p0 = fast_exp2(x0);
@@ -956,33 +970,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
         __syncwarp();
         tc_fence_after();
         if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll 1
+          for (int ch = 0; ch < 4; ++ch) {
             uint32_t o[32];
-            tmem_ld32(tl + kTmemO + ch * 32, o);
+            const uint32_t oc = tl + kTmemO + 128 * hh + ch * 32;
+            tmem_ld32(oc, o);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(tl + kTmemO + ch * 32, o);
+            tmem_st32(oc, o);
           }
         }
-        tmem_st32(tl + kTmemP, pk);
+        tmem_st16(tl + kTmemP + (kHalf / 2) * hh, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
 #pragma unroll
-        for (int c = 0; c < kTile; ++c) cur[c] = nxt[c];
+        for (int c = 0; c < kHalf; ++c) cur[c] = nxt[c];
       }
 
-      // epilogue
+      // epilogue: the row sum of both halves, then this half's 128 output dims
+      psum[hh * kRows + row] = l;
+      named_bar_pair(q4);
+      const float lt = l + psum[(1 - hh) * kRows + row];
       wait_bar(ctx, &bars->o_full, units_done & 1);
       __syncwarp();
       tc_fence_after();
-      const float inv = l > 0.f ? a.out_scale / l : 0.f;
-      const float lse_nat = l > 0.f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
-      // one row's 32 output dims (columns 32ch.. of O): bf16 output or fp32 partial
+      const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
+      const float lse_nat = lt > 0.f ? (m + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
+      // one row's 32 output dims (columns 128h + 32ch.. of O): bf16 output or fp32 partial
       auto store_chunk = [&](int ch, const uint32_t (&o)[32]) {
-        const int d0 = 256 * rank + 32 * ch;
+        const int d0 = 256 * rank + 128 * hh + 32 * ch;
         // whole 32-byte sectors per store where the address allows (a row is
         // one thread's: 16-byte stores would write half sectors)
         if (ur.slot < 0) {
@@ -1013,18 +1032,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
                          __float_as_uint(__uint_as_float(o[8 * v + 7]) * inv));
         }
       };
-      // two 32-column loads of O per wait: four round trips to TMEM, not eight
+      // two 32-column loads of O per wait
 #pragma unroll 1
-      for (int cp = 0; cp < 4; ++cp) {
+      for (int cp = 0; cp < 2; ++cp) {
         uint32_t oa[32], ob[32];
-        tmem_ld32(tl + kTmemO + cp * 64, oa);
-        tmem_ld32(tl + kTmemO + cp * 64 + 32, ob);
+        tmem_ld32(tl + kTmemO + 128 * hh + cp * 64, oa);
+        tmem_ld32(tl + kTmemO + 128 * hh + cp * 64 + 32, ob);
         tmem_wait_ld();
         if (!valid) continue;
         store_chunk(2 * cp, oa);
         store_chunk(2 * cp + 1, ob);
       }
-      if (valid && rank == 0) {
+      if (valid && rank == 0 && hh == 0) {
         if (ur.slot < 0) {
           if (a.lse) a.lse[R] = lse_nat;
         } else {
@@ -1034,35 +1053,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant == 1 
       tc_fence_before();
     }
   };
-  if constexpr (kCacheFp8 != 0) {
-    if (warp >= R::kProducer) {
-      setmaxnreg_dec<kRegsIssue>();
-      if (warp == R::kProducer)
-        producer();
-      else if (warp == R::kScore)
-        score_issuer();
-      else if (warp == R::kPV)
-        pv_issuer();
-    } else if (warp >= kWarpExpand0) {
-      setmaxnreg_dec<kRegsExpand>();
-      expander();
-    } else {
-      setmaxnreg_inc<kRegsSoftmax>();
+
+  if constexpr (kCacheFp8) {
+    // 512 threads (128 registers each at launch): each warpgroup sets its budget
+    if (warp < kSoftmaxWarps) {
+      setmaxnreg_inc<kRegsSoftmax8>();
       softmax();
+    } else if (warp < kWarpExpand0) {
+      setmaxnreg_dec<kRegsIssue8>();
+      if (warp == kWarpProducer)
+        producer();
+      else if (warp == kWarpScore)
+        score_issuer();
+      else if (warp == kWarpPV)
+        pv_issuer();
+    } else {
+      setmaxnreg_dec<kRegsExpand8>();
+      expander();
     }
   } else {
-    if (warp == R::kProducer)
-      producer();
-    else if (warp == R::kScore)
-      score_issuer();
-    else if (warp == R::kPV)
-      pv_issuer();
-    else
+    if (warp < kSoftmaxWarps)
       softmax();
+    else if (warp == kWarpProducer)
+      producer();
+    else if (warp == kWarpScore)
+      score_issuer();
+    else if (warp == kWarpPV)
+      pv_issuer();
   }
 
   __syncthreads();
-  if (warp == R::kScore) {
+  if (warp == kWarpScore) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -1089,6 +1110,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
   cfg.blockDim = dim3(variant == 1 || variant == 3 ? Roles<1>::kThreads : Roles<0>::kThreads);
+  static_assert(Roles<1>::kThreads == Roles<3>::kThreads && Roles<0>::kThreads == Roles<2>::kThreads, "roles");
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

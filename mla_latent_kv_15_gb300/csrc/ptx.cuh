@@ -369,6 +369,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 MLA_TMEM_LD64_RED(tmem_ld64_max, "max")
 MLA_TMEM_LD64_RED(tmem_ld64_min, "min")
 #undef MLA_TMEM_LD64_RED
+// the same over 32 columns
+#define MLA_TMEM_LD32_RED(NAME, OP)                                                                                    \
+  __device__ __forceinline__ void NAME(uint32_t taddr, uint32_t(&r)[32], float& red) {                                 \
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32." OP                                                          \
+                 ".f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "   \
+                 "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"                           \
+                 : MLA_R64(0), MLA_R64(1), MLA_R64(2), MLA_R64(3), MLA_R64(4), MLA_R64(5), MLA_R64(6), MLA_R64(7),    \
+                   MLA_R64(8), MLA_R64(9), MLA_R64(10), MLA_R64(11), MLA_R64(12), MLA_R64(13), MLA_R64(14),            \
+                   MLA_R64(15), MLA_R64(16), MLA_R64(17), MLA_R64(18), MLA_R64(19), MLA_R64(20), MLA_R64(21),          \
+                   MLA_R64(22), MLA_R64(23), MLA_R64(24), MLA_R64(25), MLA_R64(26), MLA_R64(27), MLA_R64(28),          \
+                   MLA_R64(29), MLA_R64(30), MLA_R64(31), "=f"(red)                                                    \
+                 : "r"(taddr)                                                                                          \
+                 : "memory");                                                                                          \
+  }
+MLA_TMEM_LD32_RED(tmem_ld32_max, "max")
+MLA_TMEM_LD32_RED(tmem_ld32_min, "min")
+#undef MLA_TMEM_LD32_RED
 #undef MLA_R64
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
