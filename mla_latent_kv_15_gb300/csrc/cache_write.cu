@@ -33,8 +33,10 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const __nv_bfloat16* _
   // Launched as a programmatic dependent: only the launch overlaps the
   // previous kernel (which may still read the cache or have written the
   // inputs); every CTA waits for it before touching memory, so the grid also
-  // completes after it.
+  // completes after it.  The next kernel may then be launched at once (its
+  // prologue overlaps this write; it waits for this grid before reading).
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t tok = blockIdx.x * 8LL + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (tok >= num_tokens) return;

@@ -436,6 +436,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       const int nsub = kTile / sub_rows;
       const int oob_row = a.num_blocks * a.page_size;  // first row past the cache: reads zeros
       const int xl = 256 * (int)rank, xr = kLkv + 32 * (int)rank;   // first latent / rope column of the CTA
+      // cache lines are read once per pair: evict them first, so that the
+      // split-KV partials, queries and block tables stay in L2
+      const uint64_t pol = l2_policy_evict_first();
       for (int u = ubeg; u < uend; ++u) {
         const UnitRec ur = P.units[u];
         const GroupRec gr = P.groups[ur.group];
@@ -458,16 +461,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
             }
             if constexpr (kQ8) {
               for (int p = 0; p < 2; ++p)
-                tma_load_2d(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, y, full);
-              tma_load_2d(dst + 2 * kQ8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full);
+                tma_load_2d_hint(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, y, full, pol);
+              tma_load_2d_hint(dst + 2 * kQ8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full, pol);
             } else if constexpr (kCacheFp8) {
               for (int p = 0; p < kVBoxes; ++p)
-                tma_load_2d(dst + p * kFp8Box + sb * sub_rows * 64, &tm_kv, xl + 64 * p, y, full);
-              tma_load_2d(dst + kVBoxes * kFp8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full);
+                tma_load_2d_hint(dst + p * kFp8Box + sb * sub_rows * 64, &tm_kv, xl + 64 * p, y, full, pol);
+              tma_load_2d_hint(dst + kVBoxes * kFp8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full, pol);
             } else {
               for (int p = 0; p < kVBoxes; ++p)
-                tma_load_2d(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, y, full);
-              tma_load_2d(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, y, full);
+                tma_load_2d_hint(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, y, full, pol);
+              tma_load_2d_hint(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, y, full, pol);
             }
           }
         };

@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   // an earlier plan) before touching memory. The decode kernel waits only for
   // this grid, which therefore also orders it after everything earlier.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the decode kernel may launch now: its prologue (barriers, TMEM, cluster
+  // sync) overlaps the plan; it waits for this grid before reading the plan
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) s_flags = 0;
   __syncthreads();
   const long long kv_cap = (long long)max_pages * page_size;
