@@ -294,8 +294,10 @@ int mla_merge_states(const void* o_a, const float* lse_a, const void* o_b, const
     return fail(MLA_ERR_INVALID_ARG, "LSE arrays must be 4-byte aligned");
   if (lse_out && (lse_out == lse_a || lse_out == lse_b))
     return fail(MLA_ERR_INVALID_ARG, "lse_out must not alias lse_a or lse_b");
+  const int sms = sm_count();   // of the current device, per call
+  if (sms < 1) return fail(MLA_ERR_CUDA, "cannot query the current device");
   cudaError_t e = mla::launch_merge_states(o_a, lse_a, o_b, lse_b, rows, dim, o_dtype == MLA_BF16, out, lse_out,
-                                           (cudaStream_t)stream);
+                                           sms, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return ok();
 }

@@ -138,7 +138,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, con
                           cudaStream_t s);
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
-                                int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,
+                                int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out, int sm_count,
                                 cudaStream_t s);
 cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
                                void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s);

@@ -7,7 +7,8 @@
 //  * merge2_kernel: the public two-way merge (mla_merge_states).
 //
 // Both are HBM-bound streaming kernels: 16-byte vector loads, one warp-slice
-// of 64 threads per 512-wide row, a grid sized in multiples of the SM count.
+// of 64 threads per 512-wide row, a grid sized in multiples of the SM count
+// (of the current device, queried by the caller on every call).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -171,17 +172,6 @@ __global__ void __launch_bounds__(256) merge2_kernel(const void* __restrict__ o_
   }
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 }  // namespace
 
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s) {
@@ -200,11 +190,11 @@ cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s) 
 }
 
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
-                                int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out,
+                                int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out, int sm_count,
                                 cudaStream_t s) {
   const int64_t nvec = rows * (dim / 8);
   int64_t blocks = (nvec + 255) / 256;
-  const int64_t cap = (int64_t)sm_count() * 8;
+  const int64_t cap = (int64_t)(sm_count > 0 ? sm_count : 1) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (o_is_bf16)
