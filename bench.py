@@ -199,7 +199,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     mla.load()
 
-    case = synth.workload(args.workload, poison=False)
+    case = synth.workload(args.workload, poison=False, **workload_overrides(args))
     N, T, B = case.num_heads, case.total_q, case.batch
     dev = "cuda"
 
@@ -384,7 +384,9 @@ def run_gpu(args):
         "dtype": "bf16" if case.cache_dtype == "bf16" else ("e4m3 q,k / bf16 p,v" if fp8q else "e4m3-cache/bf16"),
         "data": "synthetic",
         "config": {
-            "workload": args.workload, "num_heads": N, "batch": B, "total_q": T,
+            "workload": args.workload + ("" if not workload_overrides(args) else
+                                         f" (batch {B}, {case.num_blocks} pages)"),
+            "num_heads": N, "batch": B, "total_q": T,
             "ctx_sum": int(case.seq_lens.sum()), "page_size": case.page_size, "num_blocks": case.num_blocks,
             "cache_dtype": case.cache_dtype, "query": "e4m3 (scaled_fp8_quant each step)" if fp8q else "bf16",
             "num_splits": args.num_splits, "parallelism": f"replicas{world}",
@@ -436,7 +438,7 @@ def run_reference(args):
     if rank != 0:
         return None
     import oracle
-    case = synth.workload(args.workload, poison=False)
+    case = synth.workload(args.workload, poison=False, **workload_overrides(args))
     cache = oracle.prepare_cache(case)
     N = case.num_heads
     qsl = case.query_start_loc
@@ -591,7 +593,7 @@ def run_gather(args):
     import mla_latent_kv_15_gb300 as mla
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     mla.load()
-    case = synth.workload(args.workload, poison=False)
+    case = synth.workload(args.workload, poison=False, **workload_overrides(args))
     dev = "cuda"
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -691,7 +693,7 @@ def run_gather_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return None
     import oracle
-    case = synth.workload(args.workload, poison=False)
+    case = synth.workload(args.workload, poison=False, **workload_overrides(args))
     host_cache = case.pool if case.cache_dtype == "bf16" else oracle.prepare_cache(case, with_new_rows=False)
     nb = min(case.batch, 16)
     cu = np.concatenate([[0], np.cumsum(case.seq_lens.astype(np.int64))]).astype(np.int32)[:nb + 1]
@@ -759,6 +761,20 @@ def run_proj_reference(args):
     }
 
 
+def workload_overrides(args) -> dict:
+    """Request-count and page-pool overrides of a named workload (smaller
+    cases of the same shapes, e.g. for profiler captures)."""
+    over = {}
+    if getattr(args, "batch", None):
+        over["batch"] = args.batch
+        sq = synth.WORKLOADS[args.workload]["sq"]
+        if not isinstance(sq, int):
+            raise SystemExit("--batch needs a workload with one query count for every request")
+    if getattr(args, "num_blocks", None):
+        over["num_blocks"] = args.num_blocks
+    return over
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,6 +783,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3_n128_b64_ctx1k-8k", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's request count (smaller profiling captures)")
+    ap.add_argument("--num-blocks", type=int, default=None,
+                    help="override the workload's page pool (with --batch)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
