@@ -41,12 +41,19 @@ struct GroupRec {    // 32 bytes
   int tpos;          // position of its first tile on the flattened tile axis
 };
 
-struct UnitRec {     // 16 bytes
-  int group;
+// Everything a CTA pair needs to run a unit, in one 32-byte record (one
+// line, no dependent loads).
+struct UnitRec {     // 32 bytes
   int tile_begin;
   int tile_end;
   int slot;          // partial-result slot (== unit index) or -1: write the final output
+  int b;             // request
+  int row0;          // first flattened query row of the group (t*N + h)
+  int nrows;         // rows in the group
+  int lmax;          // keys visible to the group's last row
+  int kbase;         // seq_len - Sq + 1 - q0: row R sees min(kbase + R / N, lmax) keys
 };
+static_assert(sizeof(UnitRec) == 32, "unit record: one aligned 32-byte piece");
 
 struct Plan {
   PlanHeader* header;

@@ -53,7 +53,12 @@
 //    units); the final o = O / l and lse = (m + log2 l) ln 2 are exact for
 //    any reference m.  CTA 0 writes the LSE.
 //  * Split units write fp32 partials (normalised o and lse) that the combine
-//    kernel merges (merge_attn_states rule).
+//    kernel merges (merge_attn_states rule).  The epilogue stages each warp's
+//    32 rows through 4 KB of shared memory (two receive buffers the peer
+//    cannot be writing at that point) so that its global stores are whole
+//    128-byte lines.
+//  * A unit's plan record is one 32-byte line, prefetched into L1 during the
+//    epilogue of the unit before.
 //  * Every mbarrier wait is bounded (1 s unless the launch asks for less); on
 //    expiry the CTA raises its abort flag and the error word, skips its local
 //    waits and runs to the end without touching memory outside its buffers.
@@ -214,14 +219,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
-}
-
-// 32-byte global store (one whole sector); the address must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
-                                             uint32_t f, uint32_t g, uint32_t h) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
-               "r"(e), "r"(f), "r"(g), "r"(h)
-               : "memory");
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -441,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       const uint64_t pol = l2_policy_evict_first();
       for (int u = ubeg; u < uend; ++u) {
         const UnitRec ur = P.units[u];
-        const GroupRec gr = P.groups[ur.group];
+        const UnitRec& gr = ur;
         const int32_t* bt = a.block_table + (size_t)gr.b * a.max_pages;
         // loads the CTA's columns of tile j (all sub-pages) into dst, counting on `full`:
         //   bf16:           4 latent boxes of 64 x 128 B, then the 64 x 64-B rope box
@@ -708,7 +705,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
     float* pmax = pairbuf;                   // [parity][half][row]
     float* psum = pairbuf + 4 * kRows;       // [half][row]
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;   // 32-byte stores allowed
     int nrows_cur = 0;                       // rows of the current unit (the exchanged ones)
 
     // Load this half's partial scores of tile `t` from TMEM into `dst` and
@@ -814,22 +810,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       return fmaxf(v, pm[(1 - hh) * kRows + row]);
     };
 
+    // A unit's record is one 32-byte line; the epilogue of the unit before
+    // prefetches it into L1, so the load at the unit's start is short.
+    auto prefetch_unit = [&](int u) {
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(P.units + u));
+    };
+    if (ubeg < uend) prefetch_unit(ubeg);
+
     uint32_t item = 0, it = 0, units_done = 0;
     for (int u = ubeg; u < uend; ++u, ++units_done) {
       const UnitRec ur = P.units[u];
-      const GroupRec gr = P.groups[ur.group];
-      const int b = gr.b;
+      const UnitRec& gr = ur;
       nrows_cur = gr.nrows;
-      const int sq = a.qsl ? a.qsl[b + 1] - a.qsl[b] : 1;
-      const int q0 = a.qsl ? a.qsl[b] : b;
       const int R = gr.row0 + row;
       const bool valid = row < gr.nrows && R < a.total_rows;
-      // Padding rows (past the group) are never stored: they are not masked
-      // and never rescale O, so they cost a warp no work beyond the valid rows'.
+      // Keys the row may see (multi-token causal window).  Padding rows (past
+      // the group) are never stored: they are not masked and never rescale
+      // O, so they cost a warp no work beyond the valid rows'.
       int Lr = 0x7fffffff;
       if (valid) {
-        const int tloc = R / a.num_heads - q0;
-        Lr = a.seq_lens[b] - sq + 1 + tloc;
+        Lr = ur.kbase + R / a.num_heads;
         Lr = Lr < 0 ? 0 : (Lr > gr.lmax ? gr.lmax : Lr);
       }
       // the warp needs masking only on tiles that reach past its shortest valid row
@@ -993,7 +993,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         for (int c = 0; c < kHalf; ++c) cur[c] = nxt[c];
       }
 
-      // epilogue: the row sum of both halves, then this half's 128 output dims
+      if (u + 1 < uend) prefetch_unit(u + 1);
+
+      // epilogue: the row sum of both halves, then the output
       psum[hh * kRows + row] = l;
       named_bar_pair(q4);
       const float lt = l + psum[(1 - hh) * kRows + row];
@@ -1002,38 +1004,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       tc_fence_after();
       const float inv = lt > 0.f ? a.out_scale / lt : 0.f;
       const float lse_nat = lt > 0.f ? (m + __log2f(lt)) * 0.6931471805599453f : -INFINITY;
-      // one row's 32 output dims (columns 128h + 32ch.. of O): bf16 output or fp32 partial
-      auto store_chunk = [&](int ch, const uint32_t (&o)[32]) {
-        const int d0 = 256 * rank + 128 * hh + 32 * ch;
-        // whole 32-byte sectors per store where the address allows (a row is
-        // one thread's: 16-byte stores would write half sectors)
-        if (ur.slot < 0) {
-          uint32_t w[16];
+      // The rows leave through shared memory so that every store writes
+      // whole 128-byte lines (a thread owns a row: direct stores would write
+      // one 32-byte sector of 32 different lines per instruction).  The
+      // scratch of warp (q, h) is 4 KB of the receive buffer of the tile
+      // before last (h = 0) or of the last tile (h = 1): both are read, and
+      // the peer writes into them only after it has received the next
+      // unit's first tile, which this CTA sends after its epilogue.
+      const uint32_t scr = xrecv0 + ((it + 2 + (uint32_t)hh) % kXBuffers) * kXBytes + (uint32_t)q4 * 4096u;
+      // Room for the warp's 4 KB: always with 128-row buffers; a 32-row
+      // buffer (units of at most 32 rows) holds the one warp quadrant that
+      // has rows.
+      static_assert(kXRows == kRows ? 4 * 4096 <= kXBytes : 4096 <= kXBytes, "epilogue scratch");
+      const bool store = __any_sync(0xffffffffu, valid) && (kXRows == kRows || q4 == 0);
+      const int d0 = 256 * (int)rank + 128 * hh;
+      // row r of the warp (lane r's row) is stored
+      auto row_ok = [&](int r) { return q4 * 32 + r < gr.nrows && gr.row0 + q4 * 32 + r < a.total_rows; };
+      // the thread's 128 bytes -> scratch row `lane` (16-byte chunks rotated by the row: no bank conflicts)
+      auto stage = [&](const uint32_t (&w)[32]) {
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
-            w[v] = pack_bf16x2(__uint_as_float(o[2 * v]) * inv, __uint_as_float(o[2 * v + 1]) * inv);
-          __nv_bfloat16* dst = out + (size_t)R * kLkv + d0;
-          if (out32) {
-            st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-            st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
-          } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        for (int c = 0; c < 8; ++c)
+          sts128(scr + lane * 128 + ((c ^ (lane & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        __syncwarp();
+      };
+      // scratch -> global, 8 lanes per 128-byte row, 4 rows per instruction;
+      // `dst(r)` is the first byte of row r's 128 bytes
+      auto drain = [&](auto dst) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-          }
-        } else {
-          float* dst = P.part_o + ((size_t)ur.slot * kRows + row) * kLkv + d0;
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            st_global_v8(dst + 8 * v, __float_as_uint(__uint_as_float(o[8 * v]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 1]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 2]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 3]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 4]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 5]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 6]) * inv),
-                         __float_as_uint(__uint_as_float(o[8 * v + 7]) * inv));
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), c = lane & 7;
+          const uint4 v = lds128(scr + r * 128 + ((c ^ (r & 7)) << 4));
+          if (row_ok(r)) *reinterpret_cast<uint4*>(dst(r) + 16 * c) = v;
         }
+        __syncwarp();
       };
       // two 32-column loads of O per wait
 #pragma unroll 1
@@ -1042,9 +1045,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         tmem_ld32(tl + kTmemO + 128 * hh + cp * 64, oa);
         tmem_ld32(tl + kTmemO + 128 * hh + cp * 64 + 32, ob);
         tmem_wait_ld();
-        if (!valid) continue;
-        store_chunk(2 * cp, oa);
-        store_chunk(2 * cp + 1, ob);
+        if (!store) continue;
+        if (ur.slot < 0) {
+          // bf16 output: the 64 dims are one 128-byte row piece
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            oa[v] = pack_bf16x2(__uint_as_float(oa[2 * v]) * inv, __uint_as_float(oa[2 * v + 1]) * inv);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            oa[16 + v] = pack_bf16x2(__uint_as_float(ob[2 * v]) * inv, __uint_as_float(ob[2 * v + 1]) * inv);
+          stage(oa);
+          drain([&](int r) {
+            return reinterpret_cast<uint8_t*>(out + (size_t)(gr.row0 + q4 * 32 + r) * kLkv + d0 + 64 * cp);
+          });
+        } else {
+          // fp32 partial: 32 dims per 128-byte row piece
+#pragma unroll
+          for (int c = 0; c < 32; ++c) oa[c] = __float_as_uint(__uint_as_float(oa[c]) * inv);
+          stage(oa);
+          drain([&](int r) {
+            return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp);
+          });
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ob[c] = __float_as_uint(__uint_as_float(ob[c]) * inv);
+          stage(ob);
+          drain([&](int r) {
+            return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp +
+                                              32);
+          });
+        }
       }
       if (valid && rank == 0 && hh == 0) {
         if (ur.slot < 0) {

@@ -9,9 +9,9 @@
 // keys its last row may see, L = seq_len - Sq + 1 + t (multi-token causal
 // rule of the AITER MLA backend's verify path), in 64-key tiles.  Groups are
 // laid end to end on one flattened tile axis which is either
-//   * cut into equal spans, one per CTA pair (automatic: every pair gets
-//     ceil(total_tiles / clusters) tiles, a group straddling a boundary is
-//     split there), or
+//   * cut into near-equal spans, one per CTA pair (automatic: pair c gets
+//     positions [floor(c T / C), floor((c+1) T / C)) of the T on the axis,
+//     a group straddling a boundary is split there), or
 //   * with num_splits = k, every group is cut into min(k, tiles) near-equal
 //     pieces and pieces go to the pair whose span holds their midpoint.
 // Pieces of a split group write fp32 partials that the combine kernel merges
@@ -150,6 +150,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
   const int T = carry;
   const int W = T > 0 ? (T + C - 1) / C : 1;
+  // Span c of the axis is [floor(c T / Cs), floor((c+1) T / Cs)) with
+  // Cs = min(C, T) spans, none of them empty; position p lies in span
+  // floor(((p+1) Cs - 1) / T).
+  const long long Cs = T < C ? (T > 0 ? T : 1) : C;
+  auto span_start = [&](int c) { return (int)((long long)c * T / Cs); };
+  auto span_of = [&](int p) { return (int)(((long long)(p + 1) * Cs - 1) / (T > 0 ? T : 1)); };
   __syncthreads();
 
   // 3. pieces per group, unit bases
@@ -164,7 +170,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         if (num_splits > 0)
           pieces = min(num_splits, r.tiles);
         else
-          pieces = (s0 + r.tiles - 1) / W - s0 / W + 1;
+          pieces = span_of(s0 + r.tiles - 1) - span_of(s0) + 1;
       }
     }
     int total;
@@ -188,18 +194,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   for (int g = tid; g < G; g += 1024) {
     const GroupRec r = grp[g];
     const int s0 = r.tpos + kUnitCostTiles;       // first real tile on the axis
+    int kbase = 0;
+    if (r.pieces > 0) {
+      const int sq = qsl ? qsl[r.b + 1] - qsl[r.b] : 1;
+      const int q0 = qsl ? qsl[r.b] : r.b;
+      const long long seq = min((long long)seq_lens[r.b], kv_cap);
+      kbase = (int)(seq - sq + 1 - q0);
+    }
     for (int i = 0; i < r.pieces; ++i) {
       UnitRec u;
       int cl;
-      u.group = g;
+      u.b = r.b;
+      u.row0 = r.row0;
+      u.nrows = r.nrows;
+      u.lmax = r.lmax;
+      u.kbase = kbase;
       if (num_splits > 0) {
         u.tile_begin = (int)((long long)i * r.tiles / r.pieces);
         u.tile_end = (int)((long long)(i + 1) * r.tiles / r.pieces);
-        cl = min(C - 1, (s0 + (u.tile_begin + u.tile_end) / 2) / W);
+        cl = min(C - 1, span_of(s0 + (u.tile_begin + u.tile_end) / 2));
       } else {
-        cl = s0 / W + i;
-        u.tile_begin = max(s0, cl * W) - s0;
-        u.tile_end = min(s0 + r.tiles, (cl + 1) * W) - s0;
+        cl = span_of(s0) + i;
+        u.tile_begin = max(s0, span_start(cl)) - s0;
+        u.tile_end = min(s0 + r.tiles, span_start(cl + 1)) - s0;
       }
       u.slot = r.pieces > 1 ? r.ubase + i : -1;
       P.units[r.ubase + i] = u;
