@@ -280,6 +280,15 @@ __device__ __forceinline__ float max64(const float (&x)[kTile]) {
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
+// Maximum of 32 values (NaN entries are ignored: max returns the other operand).
+__device__ __forceinline__ float max_tree32(const float (&x)[32]) {
+  float m[11];
+#pragma unroll
+  for (int c = 0; c < 10; ++c) m[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
+  m[10] = fmaxf(x[30], x[31]);
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmax3(m[6], m[7], fmax3(m[8], m[9], m[10])));
+}
+
 // Maximum and minimum over the first n of 32 values (n < 32: the last,
 // ragged tile of a row; the other values are left out); NaN if n <= 0.
 __device__ __forceinline__ void range_first_n(const float (&x)[kTile / 2], int n, float& hi, float& lo) {
@@ -739,38 +748,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
     // over its visible keys), then the header (c, step) of the half.  16-byte
     // st.async stores that count against the peer's barrier (this keeps the
     // exchange off the TMA engine that streams the cache tiles).
-    auto send_s = [&](uint32_t t, const float (&src)[kHalf], int nvis, float hi, float lo) {
-      const uint32_t b = t % kXBuffers;
+    // The encoding of a half: c, step, 1/step and the FMA offset.
+    struct Enc {
+      float ctr, step, inv, off;
+    };
+    auto make_enc = [&](const float (&src)[kHalf], int nvis, float hi, float lo) {
+      if (nvis < kHalf) range_first_n(src, nvis, hi, lo);
+      if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this half
+      Enc e;
+      e.ctr = 0.5f * (hi + lo);
+      const float half = fmaxf(fmaxf(hi - e.ctr, e.ctr - lo), 1e-30f);
+      e.step = half * (1.f / kCodeRange);
+      e.inv = __fdividef(kCodeRange, half);
+      // code + 32768 = s * inv + (magic - c * inv), rounded to an integer by
+      // the FMA (within 1.5 steps of the exact code)
+      e.off = kCodeMagic - e.ctr * e.inv;
+      return e;
+    };
+    // chunk c (keys 8c..8c+7 of the half) of tile t, valid rows only
+    auto send_chunk = [&](uint32_t t, const float (&src)[kHalf], const Enc& e, int c) {
       if (row < nrows_cur) {
-        if (nvis < kHalf) range_first_n(src, nvis, hi, lo);
-        if (!(hi >= lo)) hi = lo = 0.f;      // no visible key in this half
-        const float ctr = 0.5f * (hi + lo);
-        const float half = fmaxf(fmaxf(hi - ctr, ctr - lo), 1e-30f);
-        const float step = half * (1.f / kCodeRange);
-        const float inv = __fdividef(kCodeRange, half);
-        // code + 32768 = s * inv + (magic - c * inv), rounded to an integer by
-        // the FMA (within 1.5 steps of the exact code)
-        const float off = kCodeMagic - ctr * inv;
-        const uint32_t base = xrecv_peer0 + b * kXBytes + xcode;
-        const uint32_t bar = xfull_peer0 + b * 8;
+        const uint32_t b = t % kXBuffers;
+        uint32_t w[4];
 #pragma unroll
-        for (int c = 0; c < kHalf / 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float f0, f1;
-            fma2(f0, f1, src[8 * c + 2 * j], src[8 * c + 2 * j + 1], inv, off);
-            w[j] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
-          }
-          st_async_v4(base + c * kXChunk, w[0], w[1], w[2], w[3], bar);
+        for (int j = 0; j < 4; ++j) {
+          float f0, f1;
+          fma2(f0, f1, src[8 * c + 2 * j], src[8 * c + 2 * j + 1], e.inv, e.off);
+          w[j] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x5410);
         }
-        st_async_v2(xrecv_peer0 + b * kXBytes + xhdr, __float_as_uint(ctr), __float_as_uint(step), bar);
+        st_async_v4(xrecv_peer0 + b * kXBytes + xcode + c * kXChunk, w[0], w[1], w[2], w[3], xfull_peer0 + b * 8);
       }
+    };
+    auto send_hdr = [&](uint32_t t, const Enc& e) {
+      if (row < nrows_cur) {
+        const uint32_t b = t % kXBuffers;
+        st_async_v2(xrecv_peer0 + b * kXBytes + xhdr, __float_as_uint(e.ctr), __float_as_uint(e.step),
+                    xfull_peer0 + b * 8);
+      }
+    };
+    auto send_s = [&](uint32_t t, const float (&src)[kHalf], int nvis, float hi, float lo) {
+      const Enc e = make_enc(src, nvis, hi, lo);
+#pragma unroll
+      for (int c = 0; c < kHalf / 8; ++c) send_chunk(t, src, e, c);
+      send_hdr(t, e);
     };
     // Add the peer's partial scores of this half of tile `t`, less the
     // half's centre c, into `acc`; returns c (the caller folds it into the
-    // maximum and the exponent).
-    auto recv_s = [&](uint32_t t, float (&acc)[kHalf], uint32_t nbytes) -> float {
+    // maximum and the exponent) and sets `amax` to the largest sum (computed
+    // before the barrier, where it overlaps the wait).  `between(c)` runs
+    // after chunk c is decoded (the caller sends the next tile's first
+    // chunks there, so the network transfer overlaps the decoding).
+    auto recv_s = [&](uint32_t t, float (&acc)[kHalf], uint32_t nbytes, float& amax, auto&& between) -> float {
       const uint32_t b = t % kXBuffers, use = t / kXBuffers;
       if (tid == 0) mbar_expect_tx(smem_u32(&bars->x_full[b]), nbytes);
       wait_bar_cluster(ctx, &bars->x_full[b], use & 1);
@@ -792,24 +820,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
             add2(f0, f1, -kCodeMagic, -kCodeMagic);                           // the code, exactly
             fma2v(acc[8 * c + 2 * j], acc[8 * c + 2 * j + 1], f0, f1, step);
           }
+          between(c);
         }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kHalf / 8; ++c) between(c);
       }
+      amax = max_tree32(acc);
       // every row of buffer b is read before any thread sends its row of a
       // later tile: a received tile then proves the peer is done with the
       // buffer three tiles back, whatever the row counts of the units
       named_bar_softmax();
       return ctr;
     };
-    // Maximum of the two halves' values of a row (pair exchange through
-    // shared memory; the parity alternates so that a write never meets a
-    // read of the previous exchange).
-    auto pair_max = [&](float v, uint32_t parity) {
-      float* pm = pmax + parity * 2 * kRows;
-      pm[hh * kRows + row] = v;
-      named_bar_pair(q4);
-      return fmaxf(v, pm[(1 - hh) * kRows + row]);
-    };
-
     // A unit's record is one 32-byte line; the epilogue of the unit before
     // prefetches it into L1, so the load at the unit's start is short.
     auto prefetch_unit = [&](int u) {
@@ -925,48 +948,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         send_s(it, cur, nvis(0), hi, lo);
       }
       for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
-        // exchange of the next tile first: the network copy overlaps this tile's work
-        if (jj + 1 < ntiles) {
+        // The next tile's partials are loaded first and sent in pieces while
+        // this tile is processed: chunks 0-1 between the decoding steps of
+        // this tile's received partials, chunks 2-3 and the header after its
+        // exponentials, so the network transfer overlaps the arithmetic.
+        const bool has_next = jj + 1 < ntiles;
+        Enc en{};
+        if (has_next) {
           float hi, lo;
           load_s(it + 1, nxt, hi, lo);
-          send_s(it + 1, nxt, nvis(jj + 1), hi, lo);
+          en = make_enc(nxt, nvis(jj + 1), hi, lo);
         }
-        const float cpeer = recv_s(it, cur, nbytes);   // cur = own + peer partial - cpeer
+        float hmax;
+        // cur = own + peer partial - cpeer
+        const float cpeer = recv_s(it, cur, nbytes, hmax, [&](int c) {
+          if (has_next && c < 2) send_chunk(it + 1, nxt, en, c);
+        });
 
-        // mask on ragged tiles, max of the unscaled scores of both halves
-        // (the scale is positive), then exp2(scale * s - m) as one FMA
+        // mask on ragged tiles (and take the max again), the max of the
+        // unscaled scores of both halves (the scale is positive), then
+        // exp2(scale * s - m) as one FMA
         const int key0 = (ur.tile_begin + jj) * kTile + kHalf * hh;
         if (key0 + kHalf > lmin_warp) {
 #pragma unroll
           for (int c = 0; c < kHalf; ++c) cur[c] = (key0 + c < Lr) ? cur[c] : -INFINITY;
+          hmax = max_tree32(cur);
         }
-        float mx[11];
+        // P with the current reference, computed before the halves agree on
+        // the tile maximum so that their barrier overlaps the exponentials;
+        // recomputed if the maximum moves past the lazy threshold (the first
+        // tile of a unit, or a new largest score)
+        uint32_t pk[kHalf / 2];
+        float lsum;
+        auto exp_tile = [&](float mref) {
+          const float kexp = fmaf(cpeer, a.scale_log2, -mref);   // exponent offset of this half
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 10; ++c) mx[c] = fmax3(cur[3 * c], cur[3 * c + 1], cur[3 * c + 2]);
-        mx[10] = fmaxf(cur[30], cur[31]);
-        const float hmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmax3(mx[6], mx[7], fmax3(mx[8], mx[9], mx[10])));
-        const float tmax = pair_max((hmax + cpeer) * a.scale_log2, it & 1);
+          for (int c = 0; c < kHalf / 2; ++c) {
+            float x0, x1;
+            fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, kexp);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
+            add2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], p0, p1);
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        };
+        // the halves' maxima are exchanged through shared memory; the parity
+        // alternates so that a write never meets a read of the previous tile
+        float* pm = pmax + (it & 1) * 2 * kRows;
+        const float own = (hmax + cpeer) * a.scale_log2;
+        pm[hh * kRows + row] = own;
+        exp_tile(m == -INFINITY ? 0.f : m);
+        named_bar_pair(q4);
+        const float tmax = fmaxf(own, pm[(1 - hh) * kRows + row]);
         float alpha = 1.f;
         if (valid && tmax > m + kRescaleThreshold) {
           alpha = fast_exp2(m - tmax);  // m = -inf -> 0
           l *= alpha;
           m = tmax;
+          exp_tile(m);
         }
-        const float mref = m == -INFINITY ? 0.f : m;
-        const float kexp = fmaf(cpeer, a.scale_log2, -mref);   // exponent offset of this half
-        uint32_t pk[kHalf / 2];
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kHalf / 2; ++c) {
-          float x0, x1;
-          fma2(x0, x1, cur[2 * c], cur[2 * c + 1], a.scale_log2, kexp);
-          const float p0 = fast_exp2(x0);
-          const float p1 = fast_exp2(x1);
-          add2(ls[2 * (c & 1)], ls[2 * (c & 1) + 1], p0, p1);
-          pk[c] = pack_bf16x2(p0, p1);
+        l += lsum;
+        if (has_next) {
+          send_chunk(it + 1, nxt, en, 2);
+          send_chunk(it + 1, nxt, en, 3);
+          send_hdr(it + 1, en);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
         // P and O may be touched once the P.V of the previous tile has completed
         wait_bar(ctx, &bars->p_free, (it & 1) ^ 1);
