@@ -243,7 +243,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   e = mla::launch_decode(tm_q, tm_qr, tm_kv, tm_kvr, variant, a, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
-  e = mla::launch_combine(a, L.max_groups, s);
+  e = mla::launch_combine(a, L.max_groups, sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return ok();
 }

@@ -143,7 +143,8 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
                           const CUtensorMap& tm_kvr, int variant, const DecodeArgs& a, int num_clusters,
                           cudaStream_t s);
-cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s);
+// sm_count: of the current device (the combine runs one wave of blocks)
+cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                                 int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out, int sm_count,
                                 cudaStream_t s);

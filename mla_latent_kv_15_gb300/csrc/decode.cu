@@ -422,6 +422,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
 
   // everything above overlaps the plan kernel (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the combine kernel may launch now (its blocks take SMs as CTAs of this
+  // grid finish; it waits for the whole grid before reading the partials)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ubeg = P.cluster_begin[cluster];
   const int uend = P.cluster_begin[cluster + 1];
 

@@ -16,90 +16,99 @@
 namespace mla {
 namespace {
 
-// Grid (groups, 32): block (g, y) merges rows 4y..4y+3 of group g, 64
-// threads per row, 8 dims per thread.
+// Merge of the split groups' partials.  One wave of blocks (the grid is a
+// few blocks per SM) strides over the work items (group, rows 4y..4y+3), 64
+// threads per row and 8 dims per thread; the next item's group record is
+// loaded while the current item is merged, so each item costs one round
+// trip to memory (a grid of one block per item ran in several waves of
+// blocks that each waited for two dependent loads).
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
   // launched as a programmatic dependent of the decode kernel: wait for it
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may launch (it waits for this grid)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Plan& P = a.plan;
-  const int g = blockIdx.x;
-  // both loads at once (the grid covers the workspace's max_groups records)
-  const int num_groups = P.header->num_groups;
-  const GroupRec gr = P.groups[g];
-  if (g >= num_groups) return;
-  if (gr.pieces == 1) return;  // written directly by the decode kernel
-  const int r = blockIdx.y * 4 + (threadIdx.x >> 6);
-  if (r >= gr.nrows) return;
-  const int R = gr.row0 + r;
-  if (R >= a.total_rows) return;
+  const int items = P.header->num_groups * (kRows / 4);
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
   const int sub = threadIdx.x & 63;        // 8 dims per thread
   const int d0 = sub * 8;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float lse = -INFINITY;
-  constexpr int kFew = 4;
-  if (gr.pieces <= kFew) {
-    // the usual case: every load of every piece issued before any use
-    float l[kFew];
-    float4 x0[kFew], x1[kFew];
-#pragma unroll
-    for (int i = 0; i < kFew; ++i) {
-      l[i] = -INFINITY;
-      if (i < gr.pieces) {
-        const size_t slot = (size_t)(gr.ubase + i);
-        l[i] = P.part_lse[slot * kRows + r];
-        const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
-        x0[i] = src[0];
-        x1[i] = src[1];
-      }
-    }
-    float mx = l[0];
-#pragma unroll
-    for (int i = 1; i < kFew; ++i) mx = fmaxf(mx, l[i]);
-    if (mx != -INFINITY) {
-      float wsum = 0.f;
+  int item = blockIdx.x;
+  GroupRec gnext{};
+  if (item < items) gnext = P.groups[item / (kRows / 4)];
+  for (; item < items; item += gridDim.x) {
+    const GroupRec gr = gnext;
+    if (item + (int)gridDim.x < items) gnext = P.groups[(item + gridDim.x) / (kRows / 4)];
+    if (gr.pieces == 1) continue;  // written directly by the decode kernel
+    const int r = (item % (kRows / 4)) * 4 + (threadIdx.x >> 6);
+    if (r >= gr.nrows) continue;
+    const int R = gr.row0 + r;
+    if (R >= a.total_rows) continue;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float lse = -INFINITY;
+    constexpr int kFew = 4;
+    if (gr.pieces <= kFew) {
+      // the usual case: every load of every piece issued before any use
+      float l[kFew];
+      float4 x0[kFew], x1[kFew];
 #pragma unroll
       for (int i = 0; i < kFew; ++i) {
+        l[i] = -INFINITY;
         if (i < gr.pieces) {
-          const float w = __expf(l[i] - mx);
-          wsum += w;
-          acc[0] += w * x0[i].x; acc[1] += w * x0[i].y; acc[2] += w * x0[i].z; acc[3] += w * x0[i].w;
-          acc[4] += w * x1[i].x; acc[5] += w * x1[i].y; acc[6] += w * x1[i].z; acc[7] += w * x1[i].w;
+          const size_t slot = (size_t)(gr.ubase + i);
+          l[i] = P.part_lse[slot * kRows + r];
+          const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
+          x0[i] = src[0];
+          x1[i] = src[1];
         }
       }
-      const float inv = 1.f / wsum;
+      float mx = l[0];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] *= inv;
-      lse = mx + __logf(wsum);
-    }
-  } else {
-    float mx = -INFINITY;
-    for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
-    if (mx != -INFINITY) {
-      float wsum = 0.f;
-      for (int i = 0; i < gr.pieces; ++i) {
-        const size_t slot = (size_t)(gr.ubase + i);
-        const float w = __expf(P.part_lse[slot * kRows + r] - mx);
-        wsum += w;
-        const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
-        const float4 x0 = src[0], x1 = src[1];
-        acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-        acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+      for (int i = 1; i < kFew; ++i) mx = fmaxf(mx, l[i]);
+      if (mx != -INFINITY) {
+        float wsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kFew; ++i) {
+          if (i < gr.pieces) {
+            const float w = __expf(l[i] - mx);
+            wsum += w;
+            acc[0] += w * x0[i].x; acc[1] += w * x0[i].y; acc[2] += w * x0[i].z; acc[3] += w * x0[i].w;
+            acc[4] += w * x1[i].x; acc[5] += w * x1[i].y; acc[6] += w * x1[i].z; acc[7] += w * x1[i].w;
+          }
+        }
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] *= inv;
+        lse = mx + __logf(wsum);
       }
-      const float inv = 1.f / wsum;
+    } else {
+      float mx = -INFINITY;
+      for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
+      if (mx != -INFINITY) {
+        float wsum = 0.f;
+        for (int i = 0; i < gr.pieces; ++i) {
+          const size_t slot = (size_t)(gr.ubase + i);
+          const float w = __expf(P.part_lse[slot * kRows + r] - mx);
+          wsum += w;
+          const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
+          const float4 x0 = src[0], x1 = src[1];
+          acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+          acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+        }
+        const float inv = 1.f / wsum;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] *= inv;
-      lse = mx + __logf(wsum);
+        for (int k = 0; k < 8; ++k) acc[k] *= inv;
+        lse = mx + __logf(wsum);
+      }
     }
+    uint4 v;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(acc[2], acc[3]); v.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(acc[4], acc[5]); v.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
+    *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
+    if (a.lse && sub == 0) a.lse[R] = lse;
   }
-  uint4 v;
-  __nv_bfloat162 h;
-  h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(acc[2], acc[3]); v.y = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(acc[4], acc[5]); v.z = *reinterpret_cast<uint32_t*>(&h);
-  h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
-  *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
-  if (a.lse && sub == 0) a.lse[R] = lse;
 }
 
 template <bool kBf16>
@@ -174,9 +183,14 @@ __global__ void __launch_bounds__(256) merge2_kernel(const void* __restrict__ o_
 
 }  // namespace
 
-cudaError_t launch_combine(const DecodeArgs& a, int max_groups, cudaStream_t s) {
+cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(max_groups, kRows / 4);
+  // one wave: four blocks per SM, or fewer when the plan cannot hold as many items
+  const long long max_items = (long long)max_groups * (kRows / 4);
+  long long blocks = (long long)(sm_count > 0 ? sm_count : 1) * 4;
+  if (blocks > max_items) blocks = max_items;
+  if (blocks < 1) blocks = 1;
+  cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(256);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -32,7 +32,10 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
   return v;
 }
 
-// Exclusive scan over the block (blockDim.x == 1024); *total gets the sum.
+// Threads of the plan block: a small block keeps its barriers short (a
+// batch of up to this many requests is one pass of every phase).
+constexpr int kPlanThreads = 256;
+// Exclusive scan over the block (blockDim.x == kPlanThreads); *total gets the sum.
 constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
 // Fixed cost of a work unit in tiles of decode time: loading the group's
 // query into tensor memory, refilling the pipeline and the epilogue (measured
@@ -51,7 +54,7 @@ __device__ int block_excl_scan(int v, int* total) {
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < kPlanThreads / 32 ? warp_sums[lane] : 0;
     int wi = warp_incl_scan(w);
     warp_sums[lane] = wi - w;
     if (lane == 31) s_total = wi;
@@ -67,11 +70,12 @@ __device__ int block_excl_scan(int v, int* total) {
 // the plan is built (each phase reads what other threads wrote in the
 // previous one) and are copied out at the end; for plans that fit.
 template <bool kStaged>
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens,
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ qsl, int batch, int N,
                                                     int max_pages, int page_size, int num_splits, int C,
                                                     int GR, Plan P) {
   __shared__ int s_flags;
+  __shared__ int s_span[kMaxClusters + 1];   // first axis position of every span
   __shared__ GroupRec s_groups[kStaged ? kPlanSmemGroups : 1];
   __shared__ int s_ucl[kStaged ? kPlanSmemUnits : 1];
   GroupRec* grp = kStaged ? s_groups : P.groups;
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
   // 1. groups of every request
   int carry = 0;
-  for (int base = 0; base < batch; base += 1024) {
+  for (int base = 0; base < batch; base += kPlanThreads) {
     const int b = base + tid;
     int sq = 0, ng = 0;
     if (b < batch) {
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   // 2. positions on the balanced axis: every group with keys spans its
   //    virtual unit-cost tiles, then its real tiles
   carry = 0;
-  for (int base = 0; base < G; base += 1024) {
+  for (int base = 0; base < G; base += kPlanThreads) {
     const int g = base + tid;
     const int tl = g < G ? grp[g].tiles : 0;
     const int t = tl > 0 ? tl + kUnitCostTiles : 0;
@@ -151,16 +155,24 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   const int T = carry;
   const int W = T > 0 ? (T + C - 1) / C : 1;
   // Span c of the axis is [floor(c T / Cs), floor((c+1) T / Cs)) with
-  // Cs = min(C, T) spans, none of them empty; position p lies in span
-  // floor(((p+1) Cs - 1) / T).
-  const long long Cs = T < C ? (T > 0 ? T : 1) : C;
-  auto span_start = [&](int c) { return (int)((long long)c * T / Cs); };
-  auto span_of = [&](int p) { return (int)(((long long)(p + 1) * Cs - 1) / (T > 0 ? T : 1)); };
+  // Cs = min(C, T) spans, none of them empty.  The span starts are computed
+  // once (one 64-bit division per thread); the span of a position is a
+  // float estimate corrected against them.
+  const int Cs = T < C ? (T > 0 ? T : 1) : C;
+  for (int c = tid; c <= Cs; c += kPlanThreads) s_span[c] = (int)((long long)c * T / Cs);
+  const float span_per_pos = T > 0 ? (float)Cs / (float)T : 0.f;
+  auto span_start = [&](int c) { return s_span[c]; };
+  auto span_of = [&](int p) {
+    int c = min(Cs - 1, max(0, (int)((float)p * span_per_pos)));
+    while (c > 0 && s_span[c] > p) --c;
+    while (c < Cs - 1 && s_span[c + 1] <= p) ++c;
+    return c;
+  };
   __syncthreads();
 
   // 3. pieces per group, unit bases
   carry = 0;
-  for (int base = 0; base < G; base += 1024) {
+  for (int base = 0; base < G; base += kPlanThreads) {
     const int g = base + tid;
     int pieces = 0;
     if (g < G) {
@@ -184,14 +196,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   int U = carry;
   if (U > P.max_units) {  // cannot happen for a workspace sized for num_splits
     __syncthreads();
-    for (int g = tid; g < G; g += 1024) grp[g].pieces = 0;
+    for (int g = tid; g < G; g += kPlanThreads) grp[g].pieces = 0;
     if (tid == 0) atomicOr(&s_flags, 8);
     U = 0;
   }
   __syncthreads();
 
   // 4. units
-  for (int g = tid; g < G; g += 1024) {
+  for (int g = tid; g < G; g += kPlanThreads) {
     const GroupRec r = grp[g];
     const int s0 = r.tpos + kUnitCostTiles;       // first real tile on the axis
     int kbase = 0;
@@ -226,14 +238,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   __syncthreads();
 
   // 5. first unit of every cluster (unit clusters are non-decreasing)
-  for (int u = tid; u < U; u += 1024) {
+  for (int u = tid; u < U; u += kPlanThreads) {
     const int c = ucl[u];
     const int cp = u > 0 ? ucl[u - 1] : -1;
     for (int k = cp + 1; k <= c; ++k) P.cluster_begin[k] = u;
     if (kStaged) P.unit_cluster[u] = c;
   }
   if (kStaged)
-    for (int g = tid; g < G; g += 1024) P.groups[g] = grp[g];
+    for (int g = tid; g < G; g += kPlanThreads) P.groups[g] = grp[g];
   if (tid == 0) {
     const int last = U > 0 ? ucl[U - 1] : -1;
     for (int k = last + 1; k <= kMaxClusters; ++k) P.cluster_begin[k] = U;
@@ -255,7 +267,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(1024);
+  cfg.blockDim = dim3(kPlanThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
