@@ -146,6 +146,7 @@ constexpr uint64_t kAbortWaitNs = 1000000ull;     // bound of a peer wait once t
 static_assert(kTmemP + kTile / 2 <= 512, "TMEM columns");
 
 constexpr int kMaxStages = 5;
+constexpr int kMaxSub = 4;   // sub-pages of a tile (pages of 16 rows)
 
 struct __align__(8) Barriers {
   uint64_t kv_full[kMaxStages];
@@ -456,18 +457,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         //   bf16:           4 latent boxes of 64 x 128 B, then the 64 x 64-B rope box
         //   e4m3 (v1):      4 latent boxes of 64 x 64 B, then the 64 x 32-B rope box
         //   e4m3 query (v3): 2 latent boxes of 64 x 128 B, then the 64 x 32-B rope box
+        // cache row of sub-page sb of tile j (a block-table lookup)
+        auto lookup = [&](int j, int sb) {
+          const int key = j * kTile + sb * sub_rows;
+          const int lp = key / a.page_size;
+          int y = oob_row;                   // sub-pages past the group's last key are not read
+          if (key < gr.lmax && lp < a.max_pages) {
+            const int blk = bt[lp];
+            if (blk >= 0 && blk < a.num_blocks)
+              y = blk * a.page_size + key % a.page_size;
+            else
+              atomicOr(ctx.status, 4);
+          }
+          return y;
+        };
         auto load_tile = [&](int j, uint32_t dst, uint32_t full) {
           for (int sb = 0; sb < nsub; ++sb) {
-            const int key = j * kTile + sb * sub_rows;
-            const int lp = key / a.page_size;
-            int y = oob_row;                 // sub-pages past the group's last key are not read
-            if (key < gr.lmax && lp < a.max_pages) {
-              const int blk = bt[lp];
-              if (blk >= 0 && blk < a.num_blocks)
-                y = blk * a.page_size + key % a.page_size;
-              else
-                atomicOr(ctx.status, 4);
-            }
+            const int y = lookup(j, sb);
             if constexpr (kQ8) {
               for (int p = 0; p < 2; ++p)
                 tma_load_2d_hint(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, y, full, pol);
@@ -516,6 +522,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           // a consumer's bounded wait for it runs out
           if (a.debug_skip_tile && cluster == 0 && rank == 0 && u == ubeg && jj == 0) continue;
           const uint32_t slot = item % kStages, round = item / kStages;
+          if constexpr (kVariant == 0) {
+            // 128-row bf16 variant (four-stage ring): the block-table lookups
+            // precede the slot wait, so their latency overlaps it and the
+            // tile is issued the moment the slot frees (measured 7-9 %
+            // faster kernels on the DeepSeek-V3-shaped and multi-token
+            // batches; in the other variants the same change cost 1-9 %, so
+            // they keep the lookup after the wait)
+            int ys[kMaxSub];
+#pragma unroll
+            for (int sb = 0; sb < kMaxSub; ++sb) {
+              if (sb >= nsub) break;
+              ys[sb] = lookup(ur.tile_begin + jj, sb);
+            }
+            wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
+            const uint32_t full = smem_u32(&bars->kv_full[slot]);
+            mbar_expect_tx(full, kStageBytes);
+            const uint32_t dst = smem_u32(stages + slot * kStageBytes);
+#pragma unroll
+            for (int sb = 0; sb < kMaxSub; ++sb) {
+              if (sb >= nsub) break;
+              for (int p = 0; p < kVBoxes; ++p)
+                tma_load_2d_hint(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, ys[sb], full, pol);
+              tma_load_2d_hint(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, ys[sb], full, pol);
+            }
+            continue;
+          }
           wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
           if constexpr (!kCacheFp8) {
             const uint32_t full = smem_u32(&bars->kv_full[slot]);
