@@ -197,6 +197,9 @@ __device__ __forceinline__ void raise_error(const Ctx& c, int bit) {
 // Bounded waits on this CTA's own pipeline; once the CTA has aborted they
 // return at once.
 __device__ __forceinline__ void wait_bar(const Ctx& c, uint64_t* bar, uint32_t parity) {
+  // a completed phase is taken at once (aborted or not); the abort flag is
+  // read only when the wait would block
+  if (mbar_try_wait(smem_u32(bar), parity)) return;
   if (*(volatile int*)&c.bars->abort) return;
   if (!mbar_wait(smem_u32(bar), parity, c.limit_ns)) raise_error(c, 1);
 }
@@ -204,6 +207,7 @@ __device__ __forceinline__ void wait_bar(const Ctx& c, uint64_t* bar, uint32_t p
 // (with a 1 ms bound): the peer's stores into this CTA's receive buffers must
 // land before the CTA exits.
 __device__ __forceinline__ void wait_bar_cluster(const Ctx& c, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(smem_u32(bar), parity)) return;
   const bool aborted = *(volatile int*)&c.bars->abort;
   const uint64_t lim = aborted && c.limit_ns > kAbortWaitNs ? kAbortWaitNs : c.limit_ns;
   if (!mbar_wait_cluster(smem_u32(bar), parity, lim)) raise_error(c, 1);
