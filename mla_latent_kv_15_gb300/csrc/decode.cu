@@ -986,7 +986,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         load_s(it, cur, hi, lo);
         send_s(it, cur, nvis(0), hi, lo);
       }
-      for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
+      // One tile: `cur` holds this tile's own partials, `nxt` receives the
+      // next tile's.  With a bf16 cache the loop runs two tiles per trip with
+      // the arrays swapping roles, so no copy moves `nxt` into `cur`.
+      auto tile = [&](int jj, float (&cur)[kHalf], float (&nxt)[kHalf]) {
         // The next tile's partials are loaded first and sent in pieces while
         // this tile is processed: chunks 0-1 between the decoding steps of
         // this tile's received partials, chunks 2-3 and the header after its
@@ -1076,8 +1079,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->p_full));
+      };
+      if constexpr (kCacheFp8) {
+        // e4m3 cache: one tile per trip (the unrolled form measured 8 %
+        // slower for these variants)
+        for (int jj = 0; jj < ntiles; ++jj, ++item, ++it) {
+          tile(jj, cur, nxt);
 #pragma unroll
-        for (int c = 0; c < kHalf; ++c) cur[c] = nxt[c];
+          for (int c = 0; c < kHalf; ++c) cur[c] = nxt[c];
+        }
+      } else {
+        int jj = 0;
+        for (; jj + 1 < ntiles; jj += 2) {
+          tile(jj, cur, nxt);
+          ++item, ++it;
+          tile(jj + 1, nxt, cur);
+          ++item, ++it;
+        }
+        if (jj < ntiles) {
+          tile(jj, cur, nxt);
+          ++item, ++it;
+        }
       }
 
       if (u + 1 < uend) prefetch_unit(u + 1);
