@@ -38,11 +38,11 @@ constexpr int kPlanThreads = 256;
 // Exclusive scan over the block (blockDim.x == kPlanThreads); *total gets the sum.
 constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
 // Fixed cost of a work unit in tiles of decode time: loading the group's
-// query into tensor memory, refilling the pipeline and the epilogue (measured
-// with clock64 on the DeepSeek-V3-shaped batch: ~11.5k cycles per unit
-// against ~3350 per 64-key tile).  Each group is placed on the balanced axis
-// behind this many virtual tiles, so that CTA pairs starting more groups get
-// fewer real tiles.
+// query into tensor memory, refilling the pipeline and the epilogue (a fit of
+// every CTA's end time on the DeepSeek-V3-shaped batch: ~5 us per unit
+// against ~1.3 us per 64-key tile; 3 and 4 measured alike).  Each group is
+// placed on the balanced axis behind this many virtual tiles, so that CTA
+// pairs starting more groups get fewer real tiles.
 constexpr int kUnitCostTiles = 3;
 constexpr int kPlanSmemUnits = 2048;    // and units
 
