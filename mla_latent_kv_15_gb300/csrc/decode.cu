@@ -20,15 +20,18 @@
 //    Each CTA computes a partial score tile S_r (18 MMAs, N = 64 keys), stores
 //    it into the peer's shared memory (st.async over the cluster network), and
 //    adds the peer's partial to its own.  Nothing is computed twice.
-//  * Exchange format: 16-bit block fixed point.  Per row and tile the sender
-//    takes the range [lo, hi] of its partials over the keys the row may see
-//    and sends 16-bit codes of (s - c) / step, c = (lo + hi) / 2, step = half
-//    range / 32766, with c and step as an 8-byte row header.  The absolute
-//    error is at most step / 2 whatever the magnitude of the partials (fp16
-//    would lose 2^-11 of |s|, a problem once partials reach hundreds).  The
-//    receiver folds c into the row's maximum and the exponent's offset.
-//  * The exchange of tile i+1 is issued before tile i is processed, so the
-//    network transfer overlaps the softmax of the previous tile.  Partials
+//  * Exchange format: 16-bit block fixed point.  Per row and half tile (32
+//    keys) the sender takes the range [lo, hi] of its partials over the keys
+//    the row may see and sends 16-bit codes of (s - c) / step, c = (lo + hi)
+//    / 2, step = half range / 32766, with c and step as an 8-byte header.
+//    The absolute error is at most 1.5 steps whatever the magnitude of the
+//    partials (fp16 would lose 2^-11 of |s|, a problem once partials reach
+//    hundreds).  The receiver folds c into the row's maximum and the
+//    exponent's offset.
+//  * The next tile's codes go out while the current tile is processed: the
+//    first half between the decoding steps of the received codes, the rest
+//    after the exponentials, so the network transfer overlaps the arithmetic.
+//    Partials
 //    land in a ring of four receive buffers that needs no return handshake:
 //    a CTA writes tile i+1 into the buffer of tile i-3 only after it has
 //    received tile i-1 from the peer, and the peer sent tile i-1 only after
@@ -44,14 +47,20 @@
 //    are done with the codes; the partial scores are multiplied by
 //    q_scale * kv_scale before the exchange.
 //  * Warp roles: a TMA producer, a score-MMA issuer (+TMEM owner), a P.V-MMA
-//    issuer, four softmax / exchange / O rescale / epilogue warps (one query
-//    row per thread, the row's TMEM lane) and, for an e4m3 cache, four warps
-//    that expand e4m3 tiles to bf16 (see Roles).  Separate score and P.V
-//    issuers let the two MMA accumulation chains overlap in the tensor pipe.
+//    issuer, eight softmax / exchange / O rescale / epilogue warps (two
+//    threads per query row, each a key half of every tile and an output
+//    half of O) and, for an e4m3 cache, four warps that expand e4m3 tiles to
+//    bf16 (see Roles).  Separate score and P.V issuers let the two MMA
+//    accumulation chains overlap in the tensor pipe.
+//  * The producer looks up a tile's block-table entries before it waits for
+//    the tile's ring slot, so a freed slot is refilled at once; cache tiles
+//    are loaded with an L2 evict-first policy.
 //  * Online softmax in the exp2 domain with lazy rescaling: O and l are
 //    rescaled only when a row's running max grows by more than 8 (log2
 //    units); the final o = O / l and lse = (m + log2 l) ln 2 are exact for
-//    any reference m.  CTA 0 writes the LSE.
+//    any reference m.  The exponentials are computed with the current
+//    reference while the row's two halves exchange their tile maxima, and
+//    again only if the maximum moved.  CTA 0 writes the LSE.
 //  * Split units write fp32 partials (normalised o and lse) that the combine
 //    kernel merges (merge_attn_states rule).  The epilogue stages each warp's
 //    32 rows through 4 KB of shared memory (two receive buffers the peer
@@ -59,7 +68,9 @@
 //    128-byte lines.
 //  * A unit's plan record is one 32-byte line, prefetched into L1 during the
 //    epilogue of the unit before.
-//  * Every mbarrier wait is bounded (1 s unless the launch asks for less); on
+//  * Waits take a completed phase at once and otherwise suspend on the
+//    barrier (1 us hints).  Every mbarrier wait is bounded (1 s unless the
+//    launch asks for less); on
 //    expiry the CTA raises its abort flag and the error word, skips its local
 //    waits and runs to the end without touching memory outside its buffers.
 //    Waits for the peer's partial scores stay bounded waits even then (at most
@@ -271,18 +282,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
-}
-
-// Maximum of 64 values (NaN entries are ignored: max returns the other operand).
-__device__ __forceinline__ float max64(const float (&x)[kTile]) {
-  float m[22];
-#pragma unroll
-  for (int c = 0; c < 21; ++c) m[c] = fmax3(x[3 * c], x[3 * c + 1], x[3 * c + 2]);
-  m[21] = x[63];
-#pragma unroll
-  for (int c = 0; c < 7; ++c) m[c] = fmax3(m[3 * c], m[3 * c + 1], m[3 * c + 2]);
-  m[7] = m[21];
-  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
 // Maximum of 32 values (NaN entries are ignored: max returns the other operand).
