@@ -75,3 +75,15 @@ def test_decode_fp8q_negative_scale():
     case = synth.make_decode_case(num_heads=16, batch=4, ctx=(60, 500), page_size=64, cache_dtype="fp8", seed=46)
     case.scale = -case.scale
     run_fp8q(case)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_configuration_fp8q(seed):
+    """The randomized sweep's configurations (head counts, page sizes,
+    multi-token mixes, splits, ragged pools) through the e4m3-query decode."""
+    from test_gpu_random import draw
+    kw, splits = draw(100 + seed)
+    kw["cache_dtype"] = "fp8"
+    case = synth.make_decode_case(**kw)
+    rows = sample_rows(case, 400, seed=seed) if case.total_q * case.num_heads > 3000 else None
+    run_fp8q(case, splits, rows=rows)
