@@ -138,7 +138,7 @@ constexpr int kSoftmaxWarps = 8;
 // e4m3 cache: register budget per thread of each warpgroup (two softmax
 // groups, the producer/issuer group, the expansion group) within the 512 x 128
 // the CTA is launched with
-constexpr uint32_t kRegsSoftmax8 = 160, kRegsIssue8 = 96, kRegsExpand8 = 96;
+constexpr uint32_t kRegsSoftmax8 = 168, kRegsIssue8 = 96, kRegsExpand8 = 80;
 static_assert(128 * (2 * kRegsSoftmax8 + kRegsIssue8 + kRegsExpand8) <= 512 * 128, "register split");
 constexpr int kWarpProducer = 8, kWarpScore = 9, kWarpPV = 10, kWarpExpand0 = 12;
 constexpr int kQCols = 144;                       // 288 query dims as packed bf16 pairs
