@@ -61,14 +61,18 @@ struct Plan {
   UnitRec* units;
   int* unit_cluster;     // cluster index of each unit
   int* cluster_begin;    // [kMaxClusters + 1] first unit of each cluster
-  float* part_o;         // [max_units][128][512]
+  // split partials: row r of unit u holds fp16 codes of o / 2^e, one
+  // power-of-two scale 2^e per 32-dim chunk (e from the chunk's largest
+  // magnitude, so every finite o keeps fp16's 11 significant bits)
+  uint16_t* part_o;      // [max_units][128][512] fp16 codes
+  float* part_scale;     // [max_units][128][16] 2^e of each 32-dim chunk
   float* part_lse;       // [max_units][128]
   int max_groups;
   int max_units;
 };
 
 struct WorkspaceLayout {
-  size_t header, groups, units, unit_cluster, cluster_begin, part_o, part_lse, total;
+  size_t header, groups, units, unit_cluster, cluster_begin, part_o, part_scale, part_lse, total;
   int max_groups, max_units;
 };
 
@@ -87,7 +91,8 @@ inline WorkspaceLayout workspace_layout(int batch, int total_q, int num_heads, i
   L.units = off;         off = up(off + sizeof(UnitRec) * (size_t)mu);
   L.unit_cluster = off;  off = up(off + sizeof(int) * (size_t)mu);
   L.cluster_begin = off; off = up(off + sizeof(int) * (kMaxClusters + 1));
-  L.part_o = off;        off = up(off + sizeof(float) * (size_t)mu * kRows * kLkv);
+  L.part_o = off;        off = up(off + sizeof(uint16_t) * (size_t)mu * kRows * kLkv);
+  L.part_scale = off;    off = up(off + sizeof(float) * (size_t)mu * kRows * (kLkv / 32));
   L.part_lse = off;      off = up(off + sizeof(float) * (size_t)mu * kRows);
   L.total = off;
   return L;
@@ -101,7 +106,8 @@ inline Plan plan_from_workspace(void* ws, const WorkspaceLayout& L) {
   P.units = reinterpret_cast<UnitRec*>(p + L.units);
   P.unit_cluster = reinterpret_cast<int*>(p + L.unit_cluster);
   P.cluster_begin = reinterpret_cast<int*>(p + L.cluster_begin);
-  P.part_o = reinterpret_cast<float*>(p + L.part_o);
+  P.part_o = reinterpret_cast<uint16_t*>(p + L.part_o);
+  P.part_scale = reinterpret_cast<float*>(p + L.part_scale);
   P.part_lse = reinterpret_cast<float*>(p + L.part_lse);
   P.max_groups = L.max_groups;
   P.max_units = L.max_units;

@@ -61,8 +61,11 @@
 //    any reference m.  The exponentials are computed with the current
 //    reference while the row's two halves exchange their tile maxima, and
 //    again only if the maximum moved.  CTA 0 writes the LSE.
-//  * Split units write fp32 partials (normalised o and lse) that the combine
-//    kernel merges (merge_attn_states rule).  The epilogue stages each warp's
+//  * Split units write partials that the combine kernel merges
+//    (merge_attn_states rule): the normalised o as fp16 codes with a
+//    power-of-two scale per 32-dim chunk (the chunk's largest magnitude
+//    lands in [2^14, 2^15): 11 significant bits at any magnitude, half the
+//    bytes of fp32) and the lse in fp32.  The epilogue stages each warp's
 //    32 rows through 4 KB of shared memory (two receive buffers the peer
 //    cannot be writing at that point) so that its global stores are whole
 //    128-byte lines.
@@ -1155,20 +1158,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           drain([&](int r) {
             return reinterpret_cast<uint8_t*>(out + (size_t)(gr.row0 + q4 * 32 + r) * kLkv + d0 + 64 * cp);
           });
-        } else {
-          // fp32 partial: 32 dims per 128-byte row piece
+        } else if constexpr (kVariant == 2) {
+          // partial (see below); one maximum over both halves, the same scale
+          // stored for both: this variant's code measured faster in this form
+          float mx = 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) oa[c] = __float_as_uint(__uint_as_float(oa[c]) * inv);
+          for (int c = 0; c < 32; ++c)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(oa[c])), fabsf(__uint_as_float(ob[c]))));
+          const int ebits = (int)(__float_as_uint(mx * inv) >> 23);
+          const int mexp = min(253, 268 - ebits);
+          const float mul = inv * __int_as_float(mexp << 23);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            oa[v] = pack_f16x2(__uint_as_float(oa[2 * v]) * mul, __uint_as_float(oa[2 * v + 1]) * mul);
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            oa[16 + v] = pack_f16x2(__uint_as_float(ob[2 * v]) * mul, __uint_as_float(ob[2 * v + 1]) * mul);
           stage(oa);
           drain([&](int r) {
             return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp);
           });
+          if (valid) {
+            const float sc = __int_as_float((254 - mexp) << 23);
+            *reinterpret_cast<float2*>(P.part_scale + ((size_t)ur.slot * kRows + row) * (kLkv / 32) +
+                                       (d0 + 64 * cp) / 32) = make_float2(sc, sc);
+          }
+        } else {
+          // partial: fp16 codes of o * 2^j per 32-dim chunk, 2^j chosen from
+          // the chunk's largest magnitude so that it lands in [2^14, 2^15)
+          // (within [2^-126, 2^126] for tiny chunks), and the scale 2^-j
+          float* scale = P.part_scale + ((size_t)ur.slot * kRows + row) * (kLkv / 32) + (d0 + 64 * cp) / 32;
+          auto encode = [&](const uint32_t (&o)[32], int at) {
+            float mx = 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) ob[c] = __float_as_uint(__uint_as_float(ob[c]) * inv);
-          stage(ob);
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fabsf(__uint_as_float(o[c])));
+            const int ebits = (int)(__float_as_uint(mx * inv) >> 23);  // biased exponent of the largest |o|
+            const int mexp = min(253, 268 - ebits);                       // biased exponent of 2^j
+            const float mul = inv * __int_as_float(mexp << 23);
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              oa[at + v] = pack_f16x2(__uint_as_float(o[2 * v]) * mul, __uint_as_float(o[2 * v + 1]) * mul);
+            if (valid) scale[at / 16] = __int_as_float((254 - mexp) << 23);
+          };
+          encode(oa, 0);
+          encode(ob, 16);
+          stage(oa);
           drain([&](int r) {
-            return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp +
-                                              32);
+            return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp);
           });
         }
       }

@@ -1,105 +1,74 @@
 // LSE merge kernels (merge_attn_states of the MLA pages: combine partial
 // attention results over disjoint key sets by their log-sum-exp).
 //
-//  * combine_kernel: after a split-KV decode, merges the k fp32 partials of
-//    every split group into the final bf16 output and LSE, and zero-fills
-//    groups that see no key (o = 0, lse = -inf).
+//  * combine_kernel: after a split-KV decode, merges the k partials of every
+//    split group (fp16 codes with a power-of-two scale per 32-dim chunk, fp32
+//    LSE) into the final bf16 output and LSE, and zero-fills groups that see
+//    no key (o = 0, lse = -inf).
 //  * merge2_kernel: the public two-way merge (mla_merge_states).
 //
 // Both are HBM-bound streaming kernels: 16-byte vector loads, one warp-slice
 // of 64 threads per 512-wide row, a grid sized in multiples of the SM count
 // (of the current device, queried by the caller on every call).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
 namespace mla {
 namespace {
 
-// Merge of the split groups' partials.  One wave of blocks (the grid is a
-// few blocks per SM) strides over the work items (group, rows 4y..4y+3), 64
-// threads per row and 8 dims per thread; the next item's group record is
-// loaded while the current item is merged, so each item costs one round
-// trip to memory (a grid of one block per item ran in several waves of
-// blocks that each waited for two dependent loads).
+// Merge of the split groups' partials.  One wave of blocks (the grid is as
+// many blocks as fit on every SM at once) strides over the work items (group,
+// rows 4y..4y+3), 64 threads per row and 8 dims per thread.  The kernel is
+// bound by round trips to memory, not by bytes, so every round issues as many
+// loads as it can: two consecutive items of a block are merged together when
+// their pieces number at most kFew in all, and the group records of the next
+// round are loaded while the current one is merged.
+// acc += w * the eight fp16 codes in v (a partial's codes times w x its scale)
+__device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4 v) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __half22float2(h[k]);
+    acc[2 * k] = fmaf(w, f.x, acc[2 * k]);
+    acc[2 * k + 1] = fmaf(w, f.y, acc[2 * k + 1]);
+  }
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
-  // launched as a programmatic dependent of the decode kernel: wait for it
+  const Plan& P = a.plan;
+  constexpr int kQuads = kRows / 4;   // items per group
+  constexpr int kFew = 4;             // pieces whose loads are all in flight at once
+  const int G = (int)gridDim.x;
+  const int cap = P.max_groups * kQuads;
+  // The plan's records are complete before this grid starts: the decode
+  // kernel lets it launch only after its own wait for the plan grid.  So the
+  // header and the first records are read before the wait for the decode
+  // grid, which only the partials need.
+  int item = blockIdx.x;
+  GroupRec ga{}, gb{};
+  if (item < cap) ga = P.groups[item / kQuads];
+  if (item + G < cap) gb = P.groups[(item + G) / kQuads];
+  const int items = min(cap, P.header->num_groups * kQuads);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the next kernel on the stream may launch (it waits for this grid)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const Plan& P = a.plan;
-  const int items = P.header->num_groups * (kRows / 4);
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
   const int sub = threadIdx.x & 63;        // 8 dims per thread
   const int d0 = sub * 8;
-  int item = blockIdx.x;
-  GroupRec gnext{};
-  if (item < items) gnext = P.groups[item / (kRows / 4)];
-  for (; item < items; item += gridDim.x) {
-    const GroupRec gr = gnext;
-    if (item + (int)gridDim.x < items) gnext = P.groups[(item + gridDim.x) / (kRows / 4)];
-    if (gr.pieces == 1) continue;  // written directly by the decode kernel
-    const int r = (item % (kRows / 4)) * 4 + (threadIdx.x >> 6);
-    if (r >= gr.nrows) continue;
-    const int R = gr.row0 + r;
-    if (R >= a.total_rows) continue;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float lse = -INFINITY;
-    constexpr int kFew = 4;
-    if (gr.pieces <= kFew) {
-      // the usual case: every load of every piece issued before any use
-      float l[kFew];
-      float4 x0[kFew], x1[kFew];
-#pragma unroll
-      for (int i = 0; i < kFew; ++i) {
-        l[i] = -INFINITY;
-        if (i < gr.pieces) {
-          const size_t slot = (size_t)(gr.ubase + i);
-          l[i] = P.part_lse[slot * kRows + r];
-          const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
-          x0[i] = src[0];
-          x1[i] = src[1];
-        }
-      }
-      float mx = l[0];
-#pragma unroll
-      for (int i = 1; i < kFew; ++i) mx = fmaxf(mx, l[i]);
-      if (mx != -INFINITY) {
-        float wsum = 0.f;
-#pragma unroll
-        for (int i = 0; i < kFew; ++i) {
-          if (i < gr.pieces) {
-            const float w = __expf(l[i] - mx);
-            wsum += w;
-            acc[0] += w * x0[i].x; acc[1] += w * x0[i].y; acc[2] += w * x0[i].z; acc[3] += w * x0[i].w;
-            acc[4] += w * x1[i].x; acc[5] += w * x1[i].y; acc[6] += w * x1[i].z; acc[7] += w * x1[i].w;
-          }
-        }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] *= inv;
-        lse = mx + __logf(wsum);
-      }
-    } else {
-      float mx = -INFINITY;
-      for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
-      if (mx != -INFINITY) {
-        float wsum = 0.f;
-        for (int i = 0; i < gr.pieces; ++i) {
-          const size_t slot = (size_t)(gr.ubase + i);
-          const float w = __expf(P.part_lse[slot * kRows + r] - mx);
-          wsum += w;
-          const float4* src = reinterpret_cast<const float4*>(P.part_o + (slot * kRows + r) * kLkv + d0);
-          const float4 x0 = src[0], x1 = src[1];
-          acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-          acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
-        }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] *= inv;
-        lse = mx + __logf(wsum);
-      }
-    }
+  constexpr int kChunks = kLkv / 32;       // scales per partial row
+  const int chunk = d0 / 32;               // the thread's scale
+  const int quad_row = threadIdx.x >> 6;   // row of the item
+  // pieces loaded for a group: none when the decode kernel wrote it directly
+  auto loads = [](const GroupRec& g) { return g.pieces == 1 ? 0 : g.pieces; };
+  // the item's row R (or -1 when there is nothing to write for this thread)
+  auto row_of = [&](const GroupRec& g, int it) {
+    const int r = (it % kQuads) * 4 + quad_row;
+    if (g.pieces == 1 || r >= g.nrows || g.row0 + r >= a.total_rows) return -1;
+    return g.row0 + r;
+  };
+  auto store = [&](int R, const float (&acc)[8], float lse) {
     uint4 v;
     __nv_bfloat162 h;
     h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
@@ -108,6 +77,95 @@ __global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
     h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
     *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
     if (a.lse && sub == 0) a.lse[R] = lse;
+  };
+  while (item < items) {
+    const GroupRec g0 = ga, g1 = gb;
+    const int i0 = item, i1 = item + G;
+    const int n0 = loads(g0), n1 = i1 < items ? loads(g1) : 0;
+    const bool pair = i1 < items && n0 + n1 <= kFew;
+    // the records of the next round
+    item += pair ? 2 * G : G;
+    if (pair) {
+      ga = item < items ? P.groups[item / kQuads] : GroupRec{};
+    } else {
+      ga = gb;
+    }
+    gb = item + G < items ? P.groups[(item + G) / kQuads] : GroupRec{};
+    const int R0 = row_of(g0, i0);
+    const int R1 = pair ? row_of(g1, i1) : -1;
+    const int r0 = R0 - g0.row0, r1 = R1 - g1.row0;
+
+    if (n0 > kFew) {
+      // more pieces than registers (num_splits > kFew): one piece at a time
+      if (R0 < 0) continue;
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      float lse = -INFINITY;
+      float mx = -INFINITY;
+      for (int i = 0; i < g0.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(g0.ubase + i) * kRows + r0]);
+      if (mx != -INFINITY) {
+        float wsum = 0.f;
+        for (int i = 0; i < g0.pieces; ++i) {
+          const size_t slot = (size_t)(g0.ubase + i);
+          const float w = __expf(P.part_lse[slot * kRows + r0] - mx);
+          wsum += w;
+          const size_t at = slot * kRows + r0;
+          accumulate(acc, w * P.part_scale[at * kChunks + chunk],
+                     *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + d0));
+        }
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] *= inv;
+        lse = mx + __logf(wsum);
+      }
+      store(R0, acc, lse);
+      continue;
+    }
+
+    // every load of both items issued before any use: entries [0, n0) are
+    // the first item's pieces, [n0, n0 + n1) the second's
+    float l[kFew], sc[kFew];
+    uint4 x[kFew];
+#pragma unroll
+    for (int i = 0; i < kFew; ++i) {
+      l[i] = -INFINITY;
+      size_t at = ~(size_t)0;
+      if (R0 >= 0 && i < n0)
+        at = (size_t)(g0.ubase + i) * kRows + r0;
+      else if (R1 >= 0 && i >= n0 && i < n0 + n1)
+        at = (size_t)(g1.ubase + i - n0) * kRows + r1;
+      if (at != ~(size_t)0) {
+        l[i] = P.part_lse[at];
+        sc[i] = P.part_scale[at * kChunks + chunk];
+        x[i] = *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + d0);
+      }
+    }
+    // LSE merge of entries [lo, hi) into row R
+    auto merge = [&](int lo, int hi, int R) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kFew; ++i)
+        if (i >= lo && i < hi) mx = fmaxf(mx, l[i]);
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      float lse = -INFINITY;
+      if (mx != -INFINITY) {
+        float wsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kFew; ++i) {
+          if (i >= lo && i < hi) {
+            const float w = __expf(l[i] - mx);
+            wsum += w;
+            accumulate(acc, w * sc[i], x[i]);
+          }
+        }
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] *= inv;
+        lse = mx + __logf(wsum);
+      }
+      store(R, acc, lse);
+    };
+    if (R0 >= 0) merge(0, n0, R0);
+    if (R1 >= 0) merge(n0, n0 + n1, R1);
   }
 }
 
@@ -184,10 +242,17 @@ __global__ void __launch_bounds__(256) merge2_kernel(const void* __restrict__ o_
 }  // namespace
 
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cudaStream_t s) {
+  // one wave: as many blocks as are resident on every SM at once (a block
+  // beyond that would start only when another ends), or fewer when the plan
+  // cannot hold as many items
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, combine_kernel, 256, 0) != cudaSuccess || n < 1) n = 1;
+    return n;
+  }();
   cudaLaunchConfig_t cfg = {};
-  // one wave: four blocks per SM, or fewer when the plan cannot hold as many items
   const long long max_items = (long long)max_groups * (kRows / 4);
-  long long blocks = (long long)(sm_count > 0 ? sm_count : 1) * 4;
+  long long blocks = (long long)(sm_count > 0 ? sm_count : 1) * per_sm;
   if (blocks > max_items) blocks = max_items;
   if (blocks < 1) blocks = 1;
   cfg.gridDim = dim3((unsigned)blocks);

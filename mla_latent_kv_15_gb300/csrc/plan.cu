@@ -14,7 +14,7 @@
 //     a group straddling a boundary is split there), or
 //   * with num_splits = k, every group is cut into min(k, tiles) near-equal
 //     pieces and pieces go to the pair whose span holds their midpoint.
-// Pieces of a split group write fp32 partials that the combine kernel merges
+// Pieces of a split group write partials that the combine kernel merges
 // with the LSE rule of merge_attn_states.
 #include "common.cuh"
 

@@ -4,6 +4,8 @@ Bars: cache write and paged gather bit-exact; latent output max abs error
 <= 2e-2 (bf16 cache) or <= 6e-2 (fp8 cache, against the oracle on dequantised
 values); LSE max abs error <= 1e-3.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -15,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import mla_latent_kv_15_gb300 as mla
-    from gpu_case import GpuCase, compare, sample_rows, bf16_tensor, LKV, DQK
+    from gpu_case import GpuCase, compare, sample_rows, bf16_tensor, LKV, DQK, TOL_OUT_BF16, TOL_LSE
 
 
 # ----------------------------------------------------------------- cache write
@@ -191,7 +193,7 @@ def test_one_token_context_returns_kv_c_bitexact():
 
 def test_split_counts_agree():
     """Automatic and forced splits (1, 2, 7 pieces) give the same result within
-    the fp32 merge rounding."""
+    the rounding of the stored partials and of the merge."""
     case = synth.make_decode_case(num_heads=128, batch=5, ctx=(500, 2000), page_size=64, seed=43)
     g = GpuCase(case, num_splits_max=7)
     res = []
@@ -202,6 +204,40 @@ def test_split_counts_agree():
     for o, l in res[1:]:
         assert torch.max(torch.abs(o - res[0][0])).item() <= 1.6e-2
         assert torch.max(torch.abs(l - res[0][1])).item() <= 1e-4
+
+
+def _scale_bf16(bits: np.ndarray, k: int) -> np.ndarray:
+    """bf16 bits of x * 2^k (exact: asserted)."""
+    f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** k)
+    out = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((out.astype(np.uint32) << 16).view(np.float32), f)
+    return out
+
+
+@pytest.mark.parametrize("num_heads", [128, 16])
+@pytest.mark.parametrize("k", [20, -30])
+def test_split_partials_at_any_magnitude(num_heads, k):
+    """Split partials keep their precision whatever the values' magnitude
+    (they are stored as fp16 codes with a power-of-two scale per 32-dim
+    chunk; plain fp16 would overflow at 2^20 and lose everything at 2^-30).
+    kv_c is scaled by 2^k and q_abs by 2^-k: every score, hence the LSE, is
+    unchanged and the output scales by exactly 2^k, so 2^-k times the output
+    meets the bar against the oracle of the unscaled case."""
+    case = synth.make_decode_case(num_heads=num_heads, batch=5, ctx=(500, 2000), page_size=64, seed=45,
+                                  poison=False)
+    big = dataclasses.replace(case, pool=case.pool.copy(), new_kv_c=_scale_bf16(case.new_kv_c, k),
+                              q_abs=_scale_bf16(case.q_abs, -k))
+    big.pool[..., :LKV] = _scale_bf16(case.pool[..., :LKV], k)
+    g = GpuCase(big, num_splits_max=7)
+    ref_o, ref_lse, _ = oracle.decode_case(case, oracle.prepare_cache(case))
+    for splits in (0, 7):
+        g.decode(splits)
+        out = g.out.float().reshape(-1, LKV).cpu().numpy().astype(np.float64) * 2.0 ** -k
+        lse = g.lse.reshape(-1).cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+        assert np.max(np.abs(out - ref_o)) <= TOL_OUT_BF16
+        assert np.max(np.abs(lse - ref_lse)) <= TOL_LSE
+        assert mla.decode_status(g.workspace) == 0
 
 
 def test_block_id_out_of_range_flags_and_does_not_fault():
