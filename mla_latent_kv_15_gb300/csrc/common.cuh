@@ -137,7 +137,7 @@ struct DecodeArgs {
 };
 
 // ---- launchers (return cudaError_t of the launch)
-// group_rows: query rows per group (128; 32 for the small-rows decode variant)
+// group_rows: query rows per group, a power of two (128; 32 for the small-rows decode variant)
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s);
 // variant: 0 bf16 cache, 1 e4m3 cache, 2 bf16 cache with <= 32-row groups

@@ -35,7 +35,6 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 // Threads of the plan block: a small block keeps its barriers short (a
 // batch of up to this many requests is one pass of every phase).
 constexpr int kPlanThreads = 256;
-// Exclusive scan over the block (blockDim.x == kPlanThreads); *total gets the sum.
 constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
 // Fixed cost of a work unit in tiles of decode time: loading the group's
 // query into tensor memory, refilling the pipeline and the epilogue (a fit of
@@ -46,24 +45,36 @@ constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many group
 constexpr int kUnitCostTiles = 3;
 constexpr int kPlanSmemUnits = 2048;    // and units
 
-__device__ int block_excl_scan(int v, int* total) {
-  __shared__ int warp_sums[32];
-  __shared__ int s_total;
+// Exclusive scan over the block (blockDim.x == kPlanThreads) with one
+// barrier: every warp scans its values and publishes its total; after the
+// barrier each warp adds the totals of the warps before it.  Consecutive
+// scans alternate between the two rows of `sums`, so a warp may start the
+// next scan while another still reads this one's totals (no warp gets two
+// scans ahead: each scan has a barrier).  *total gets the block's sum.
+__device__ __forceinline__ int block_excl_scan(int v, int* total, int (&sums)[2][kPlanThreads / 32], int& row) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = warp_incl_scan(v);
-  if (lane == 31) warp_sums[warp] = incl;
+  const int incl = warp_incl_scan(v);
+  int* buf = sums[row];
+  row ^= 1;
+  if (lane == 31) buf[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < kPlanThreads / 32 ? warp_sums[lane] : 0;
-    int wi = warp_incl_scan(w);
-    warp_sums[lane] = wi - w;
-    if (lane == 31) s_total = wi;
+  int before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kPlanThreads / 32; ++w) {
+    const int x = buf[w];
+    before += w < warp ? x : 0;
+    all += x;
   }
-  __syncthreads();
-  int r = incl - v + warp_sums[warp];
-  *total = s_total;
-  __syncthreads();
-  return r;
+  *total = all;
+  return incl - v + before;
+}
+
+// floor(a * b / c) for a, b >= 0 and c > 0: a 32-bit division whenever the
+// product fits (a 64-bit division is a long chain of dependent instructions)
+__device__ __forceinline__ int muldiv(int a, int b, int c) {
+  const unsigned long long p = (unsigned long long)(unsigned)a * (unsigned)b;
+  if (p <= 0xffffffffull) return (int)((unsigned)p / (unsigned)c);
+  return (int)(p / (unsigned long long)c);
 }
 
 // kStaged: the group records and unit clusters live in shared memory while
@@ -78,6 +89,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   __shared__ int s_span[kMaxClusters + 1];   // first axis position of every span
   __shared__ GroupRec s_groups[kStaged ? kPlanSmemGroups : 1];
   __shared__ int s_ucl[kStaged ? kPlanSmemUnits : 1];
+  __shared__ int s_kbase[kStaged ? kPlanSmemGroups : 1];   // seq_len - Sq + 1 - q0 of each group's request
+  __shared__ int s_sums[2][kPlanThreads / 32];
+  int sums_row = 0;
   GroupRec* grp = kStaged ? s_groups : P.groups;
   int* ucl = kStaged ? s_ucl : P.unit_cluster;
   const int tid = threadIdx.x;
@@ -93,28 +107,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   if (tid == 0) s_flags = 0;
   __syncthreads();
   const long long kv_cap = (long long)max_pages * page_size;
+  const int gshift = __ffs(GR) - 1;   // GR is a power of two
 
   // 1. groups of every request
   int carry = 0;
   for (int base = 0; base < batch; base += kPlanThreads) {
     const int b = base + tid;
-    int sq = 0, ng = 0;
+    int sq = 0, ng = 0, q0 = 0;
+    long long seq = 0;
     if (b < batch) {
-      sq = qsl ? qsl[b + 1] - qsl[b] : 1;
+      // all of the request's loads at once
+      q0 = qsl ? qsl[b] : b;
+      sq = qsl ? qsl[b + 1] - q0 : 1;
+      seq = seq_lens[b];
       if (sq < 0) sq = 0;
-      ng = (int)(((long long)sq * N + GR - 1) / GR);
+      ng = (int)(((long long)sq * N + GR - 1) >> gshift);
     }
     int total;
-    const int gb = block_excl_scan(ng, &total) + carry;
+    const int gb = block_excl_scan(ng, &total, s_sums, sums_row) + carry;
     if (b < batch && ng > 0) {
-      const int q0 = qsl ? qsl[b] : b;
-      long long seq = seq_lens[b];
       if (seq > kv_cap) {
         atomicOr(&s_flags, 2);  // MLA_DEVERR_BAD_SEQ_LEN
         seq = kv_cap;
       }
+      const int kbase = (int)(seq - sq + 1 - q0);
       const int rows_b = sq * N;
       for (int g = 0; g < ng && gb + g < P.max_groups; ++g) {
+        if (kStaged) s_kbase[gb + g] = kbase;
         GroupRec r;
         r.b = b;
         r.row0 = q0 * N + g * GR;
@@ -148,7 +167,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     const int tl = g < G ? grp[g].tiles : 0;
     const int t = tl > 0 ? tl + kUnitCostTiles : 0;
     int total;
-    const int pos = block_excl_scan(t, &total) + carry;
+    const int pos = block_excl_scan(t, &total, s_sums, sums_row) + carry;
     if (g < G) grp[g].tpos = pos;
     carry += total;
   }
@@ -156,11 +175,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   const int W = T > 0 ? (T + C - 1) / C : 1;
   // Span c of the axis is [floor(c T / Cs), floor((c+1) T / Cs)) with
   // Cs = min(C, T) spans, none of them empty.  The span starts are computed
-  // once (one 64-bit division per thread); the span of a position is a
-  // float estimate corrected against them.
+  // once (one division per thread); the span of a position is a float
+  // estimate corrected against them.
   const int Cs = T < C ? (T > 0 ? T : 1) : C;
-  for (int c = tid; c <= Cs; c += kPlanThreads) s_span[c] = (int)((long long)c * T / Cs);
-  const float span_per_pos = T > 0 ? (float)Cs / (float)T : 0.f;
+  for (int c = tid; c <= Cs; c += kPlanThreads) s_span[c] = muldiv(c, T, Cs);
+  const float span_per_pos = T > 0 ? __fdividef((float)Cs, (float)T) : 0.f;
   auto span_start = [&](int c) { return s_span[c]; };
   auto span_of = [&](int p) {
     int c = min(Cs - 1, max(0, (int)((float)p * span_per_pos)));
@@ -186,7 +205,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       }
     }
     int total;
-    const int ub = block_excl_scan(pieces, &total) + carry;
+    const int ub = block_excl_scan(pieces, &total, s_sums, sums_row) + carry;
     if (g < G) {
       grp[g].pieces = pieces;
       grp[g].ubase = ub;
@@ -207,7 +226,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     const GroupRec r = grp[g];
     const int s0 = r.tpos + kUnitCostTiles;       // first real tile on the axis
     int kbase = 0;
-    if (r.pieces > 0) {
+    if (kStaged) {
+      kbase = s_kbase[g];
+    } else if (r.pieces > 0) {
       const int sq = qsl ? qsl[r.b + 1] - qsl[r.b] : 1;
       const int q0 = qsl ? qsl[r.b] : r.b;
       const long long seq = min((long long)seq_lens[r.b], kv_cap);
@@ -222,8 +243,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       u.lmax = r.lmax;
       u.kbase = kbase;
       if (num_splits > 0) {
-        u.tile_begin = (int)((long long)i * r.tiles / r.pieces);
-        u.tile_end = (int)((long long)(i + 1) * r.tiles / r.pieces);
+        u.tile_begin = muldiv(i, r.tiles, r.pieces);
+        u.tile_end = muldiv(i + 1, r.tiles, r.pieces);
         cl = min(C - 1, span_of(s0 + (u.tile_begin + u.tile_end) / 2));
       } else {
         cl = span_of(s0) + i;
