@@ -7,9 +7,8 @@
 //    no key (o = 0, lse = -inf).
 //  * merge2_kernel: the public two-way merge (mla_merge_states).
 //
-// Both are HBM-bound streaming kernels: 16-byte vector loads, one warp-slice
-// of 64 threads per 512-wide row, a grid sized in multiples of the SM count
-// (of the current device, queried by the caller on every call).
+// Both stream with 16-byte vector loads over a grid sized in multiples of the
+// SM count (of the current device, queried by the caller on every call).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -18,15 +17,8 @@
 namespace mla {
 namespace {
 
-// Merge of the split groups' partials.  One wave of blocks (the grid is as
-// many blocks as fit on every SM at once) strides over the work items (group,
-// rows 4y..4y+3), 64 threads per row and 8 dims per thread.  The kernel is
-// bound by round trips to memory, not by bytes, so every round issues as many
-// loads as it can: two consecutive items of a block are merged together when
-// their pieces number at most kFew in all, and the group records of the next
-// round are loaded while the current one is merged.
-// acc += w * the eight fp16 codes in v (a partial's codes times w x its scale)
-__device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4 v) {
+// acc[0..7] += w * the eight fp16 codes in v (a partial's codes times w x its scale)
+__device__ __forceinline__ void accumulate(float* acc, float w, const uint4 v) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -36,136 +28,118 @@ __device__ __forceinline__ void accumulate(float (&acc)[8], float w, const uint4
   }
 }
 
-__global__ void __launch_bounds__(256) combine_kernel(const DecodeArgs a) {
+// Merge of the split groups' partials.  The work item is (group, rows
+// 4y..4y+3); 64 threads take an item, 16 per row and 32 dims per thread
+// (dims 128c + 8s .. 128c + 8s + 7 for c = 0..3 of thread s, so that every
+// load instruction of a warp reads whole 256-byte runs), and a block of 256
+// threads holds four items at once.
+// The kernel is bound by the latency of its loads: every load of an item's
+// pieces is issued before any use, and the next item's group record loads
+// while the current one merges.  One wave of blocks (as many as are
+// resident on every SM at once) strides over the items.
+__global__ void __launch_bounds__(256, 2) combine_kernel(const DecodeArgs a) {
   const Plan& P = a.plan;
   constexpr int kQuads = kRows / 4;   // items per group
-  constexpr int kFew = 4;             // pieces whose loads are all in flight at once
-  const int G = (int)gridDim.x;
+  // pieces whose loads are all in flight at once: with the balanced split a
+  // group spans at most three CTA-pair spans unless it is longer than two
+  constexpr int kFew = 3;
+  constexpr int kChunks = kLkv / 32;  // scales per partial row
+  const int VG = (int)gridDim.x * 4;  // item slots of the grid
   const int cap = P.max_groups * kQuads;
   // The plan's records are complete before this grid starts: the decode
   // kernel lets it launch only after its own wait for the plan grid.  So the
-  // header and the first records are read before the wait for the decode
+  // header and the first record are read before the wait for the decode
   // grid, which only the partials need.
-  int item = blockIdx.x;
-  GroupRec ga{}, gb{};
-  if (item < cap) ga = P.groups[item / kQuads];
-  if (item + G < cap) gb = P.groups[(item + G) / kQuads];
+  int item = (int)blockIdx.x * 4 + (int)(threadIdx.x >> 6);
+  GroupRec gnext{};
+  if (item < cap) gnext = P.groups[item / kQuads];
   const int items = min(cap, P.header->num_groups * kQuads);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the next kernel on the stream may launch (it waits for this grid)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-  const int sub = threadIdx.x & 63;        // 8 dims per thread
+  const int sub = threadIdx.x & 15;              // dims 128 c + 8 sub .. + 7, c = 0..3
   const int d0 = sub * 8;
-  constexpr int kChunks = kLkv / 32;       // scales per partial row
-  const int chunk = d0 / 32;               // the thread's scale
-  const int quad_row = threadIdx.x >> 6;   // row of the item
-  // pieces loaded for a group: none when the decode kernel wrote it directly
-  auto loads = [](const GroupRec& g) { return g.pieces == 1 ? 0 : g.pieces; };
-  // the item's row R (or -1 when there is nothing to write for this thread)
-  auto row_of = [&](const GroupRec& g, int it) {
-    const int r = (it % kQuads) * 4 + quad_row;
-    if (g.pieces == 1 || r >= g.nrows || g.row0 + r >= a.total_rows) return -1;
-    return g.row0 + r;
-  };
-  auto store = [&](int R, const float (&acc)[8], float lse) {
-    uint4 v;
-    __nv_bfloat162 h;
-    h = __floats2bfloat162_rn(acc[0], acc[1]); v.x = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[2], acc[3]); v.y = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[4], acc[5]); v.z = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(acc[6], acc[7]); v.w = *reinterpret_cast<uint32_t*>(&h);
-    *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + d0) = v;
-    if (a.lse && sub == 0) a.lse[R] = lse;
-  };
-  while (item < items) {
-    const GroupRec g0 = ga, g1 = gb;
-    const int i0 = item, i1 = item + G;
-    const int n0 = loads(g0), n1 = i1 < items ? loads(g1) : 0;
-    const bool pair = i1 < items && n0 + n1 <= kFew;
-    // the records of the next round
-    item += pair ? 2 * G : G;
-    if (pair) {
-      ga = item < items ? P.groups[item / kQuads] : GroupRec{};
-    } else {
-      ga = gb;
-    }
-    gb = item + G < items ? P.groups[(item + G) / kQuads] : GroupRec{};
-    const int R0 = row_of(g0, i0);
-    const int R1 = pair ? row_of(g1, i1) : -1;
-    const int r0 = R0 - g0.row0, r1 = R1 - g1.row0;
-
-    if (n0 > kFew) {
-      // more pieces than registers (num_splits > kFew): one piece at a time
-      if (R0 < 0) continue;
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      float lse = -INFINITY;
-      float mx = -INFINITY;
-      for (int i = 0; i < g0.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(g0.ubase + i) * kRows + r0]);
-      if (mx != -INFINITY) {
-        float wsum = 0.f;
-        for (int i = 0; i < g0.pieces; ++i) {
-          const size_t slot = (size_t)(g0.ubase + i);
-          const float w = __expf(P.part_lse[slot * kRows + r0] - mx);
-          wsum += w;
-          const size_t at = slot * kRows + r0;
-          accumulate(acc, w * P.part_scale[at * kChunks + chunk],
-                     *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + d0));
+  const int quad_row = (threadIdx.x >> 4) & 3;   // row of the item
+  for (; item < items; item += VG) {
+    const GroupRec gr = gnext;
+    if (item + VG < items) gnext = P.groups[(item + VG) / kQuads];
+    if (gr.pieces == 1) continue;  // written directly by the decode kernel
+    const int r = (item % kQuads) * 4 + quad_row;
+    if (r >= gr.nrows || gr.row0 + r >= a.total_rows) continue;
+    const int R = gr.row0 + r;
+    float acc[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    float lse = -INFINITY;
+    if (gr.pieces <= kFew) {
+      // the usual case: every load of every piece issued before any use
+      float l[kFew], sc[kFew][4];
+      uint4 x[kFew][4];
+#pragma unroll
+      for (int i = 0; i < kFew; ++i) {
+        l[i] = -INFINITY;
+        if (i < gr.pieces) {
+          const size_t at = (size_t)(gr.ubase + i) * kRows + r;
+          l[i] = P.part_lse[at];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            sc[i][c] = P.part_scale[at * kChunks + 4 * c + (sub >> 2)];
+            x[i][c] = *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + 128 * c + d0);
+          }
         }
-        const float inv = 1.f / wsum;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] *= inv;
-        lse = mx + __logf(wsum);
       }
-      store(R0, acc, lse);
-      continue;
-    }
-
-    // every load of both items issued before any use: entries [0, n0) are
-    // the first item's pieces, [n0, n0 + n1) the second's
-    float l[kFew], sc[kFew];
-    uint4 x[kFew];
+      float mx = l[0];
 #pragma unroll
-    for (int i = 0; i < kFew; ++i) {
-      l[i] = -INFINITY;
-      size_t at = ~(size_t)0;
-      if (R0 >= 0 && i < n0)
-        at = (size_t)(g0.ubase + i) * kRows + r0;
-      else if (R1 >= 0 && i >= n0 && i < n0 + n1)
-        at = (size_t)(g1.ubase + i - n0) * kRows + r1;
-      if (at != ~(size_t)0) {
-        l[i] = P.part_lse[at];
-        sc[i] = P.part_scale[at * kChunks + chunk];
-        x[i] = *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + d0);
-      }
-    }
-    // LSE merge of entries [lo, hi) into row R
-    auto merge = [&](int lo, int hi, int R) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kFew; ++i)
-        if (i >= lo && i < hi) mx = fmaxf(mx, l[i]);
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      float lse = -INFINITY;
+      for (int i = 1; i < kFew; ++i) mx = fmaxf(mx, l[i]);
       if (mx != -INFINITY) {
         float wsum = 0.f;
 #pragma unroll
         for (int i = 0; i < kFew; ++i) {
-          if (i >= lo && i < hi) {
+          if (i < gr.pieces) {
             const float w = __expf(l[i] - mx);
             wsum += w;
-            accumulate(acc, w * sc[i], x[i]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) accumulate(acc + 8 * c, w * sc[i][c], x[i][c]);
           }
         }
         const float inv = 1.f / wsum;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] *= inv;
+        for (int k = 0; k < 32; ++k) acc[k] *= inv;
         lse = mx + __logf(wsum);
       }
-      store(R, acc, lse);
-    };
-    if (R0 >= 0) merge(0, n0, R0);
-    if (R1 >= 0) merge(n0, n0 + n1, R1);
+    } else {
+      // more pieces than registers (num_splits > kFew): one piece at a time
+      float mx = -INFINITY;
+      for (int i = 0; i < gr.pieces; ++i) mx = fmaxf(mx, P.part_lse[(size_t)(gr.ubase + i) * kRows + r]);
+      if (mx != -INFINITY) {
+        float wsum = 0.f;
+        for (int i = 0; i < gr.pieces; ++i) {
+          const size_t at = (size_t)(gr.ubase + i) * kRows + r;
+          const float w = __expf(P.part_lse[at] - mx);
+          wsum += w;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            accumulate(acc + 8 * c, w * P.part_scale[at * kChunks + 4 * c + (sub >> 2)],
+                       *reinterpret_cast<const uint4*>(P.part_o + at * kLkv + 128 * c + d0));
+        }
+        const float inv = 1.f / wsum;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] *= inv;
+        lse = mx + __logf(wsum);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 v;
+      __nv_bfloat162 h;
+      h = __floats2bfloat162_rn(acc[8 * c + 0], acc[8 * c + 1]); v.x = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2bfloat162_rn(acc[8 * c + 2], acc[8 * c + 3]); v.y = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2bfloat162_rn(acc[8 * c + 4], acc[8 * c + 5]); v.z = *reinterpret_cast<uint32_t*>(&h);
+      h = __floats2bfloat162_rn(acc[8 * c + 6], acc[8 * c + 7]); v.w = *reinterpret_cast<uint32_t*>(&h);
+      *reinterpret_cast<uint4*>(out + (size_t)R * kLkv + 128 * c + d0) = v;
+    }
+    if (a.lse && sub == 0) a.lse[R] = lse;
   }
 }
 
@@ -253,7 +227,7 @@ cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cu
   cudaLaunchConfig_t cfg = {};
   const long long max_items = (long long)max_groups * (kRows / 4);
   long long blocks = (long long)(sm_count > 0 ? sm_count : 1) * per_sm;
-  if (blocks > max_items) blocks = max_items;
+  if (blocks * 4 > max_items) blocks = (max_items + 3) / 4;   // four items per block at once
   if (blocks < 1) blocks = 1;
   cfg.gridDim = dim3((unsigned)blocks);
   cfg.blockDim = dim3(256);
