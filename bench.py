@@ -286,12 +286,21 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
         host_lead(stream)
-        for i in range(args.steps):
-            if do_flush:
+        if do_flush:
+            # the flush between steps stays outside the timed intervals
+            for i in range(args.steps):
                 flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            step(d)
-            ev[i][1].record(stream)
+                ev[i][0].record(stream)
+                step(d)
+                ev[i][1].record(stream)
+        else:
+            # one event pair around the K back-to-back steps: an event recorded
+            # between two steps would sit between the combine of one and the
+            # cache write of the next, which could then no longer launch early
+            ev[0][0].record(stream)
+            for i in range(args.steps):
+                step(d)
+            ev[0][1].record(stream)
         torch.cuda.synchronize()
         host_lead(stream)
         for i in range(args.steps):
@@ -303,19 +312,23 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
+    if do_flush:
+        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    else:
+        ms = ev[0][0].elapsed_time(ev[0][1]) / args.steps
     kern_ms = [a.elapsed_time(b) for a, b in kev]
-    ms = sum(step_ms) / len(step_ms)
     kms = sum(kern_ms) / len(kern_ms)
 
     # ---- e2e: every step copies its inputs in from pinned host memory and
     # reads its outputs back: the inputs as one packed pinned buffer (one
     # copy), the output and LSE as one packed device buffer (one copy back).
-    # Two buffer sets: step i+1's inputs travel on a copy stream while step i
-    # computes, step i's outputs on another after it.  A spin kernel ahead of
-    # the timed region lets the host enqueue ahead, as for the device-resident
-    # timing.  The KV cache (hundreds of MB per step) is larger than L2, so no
-    # flush.
+    # Steps run in groups of G back to back: group g+1's inputs travel on a
+    # copy stream while group g computes, and group g's outputs travel back
+    # on another after it (2G device buffer sets).  The compute stream waits
+    # once per group, so within a group every kernel may still launch under
+    # the one before it.  A spin kernel ahead of the timed region lets the
+    # host enqueue ahead, as for the device-resident timing.  The KV cache
+    # (hundreds of MB per step) is larger than L2, so no flush.
     def nbytes(t):
         return t.numel() * t.element_size()
 
@@ -329,45 +342,57 @@ def run_gpu(args):
     def views(buf, tensors, offs):
         return {k: buf[offs[k]:offs[k] + nbytes(t)].view(t.dtype).view(t.shape) for k, t in tensors.items()}
 
+    G = max(1, min(args.e2e_group, args.steps))
+    NB = 2 * G
     in_offs, in_total = layout(host)
     h_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
     for k, t in host.items():
         h_in[in_offs[k]:in_offs[k] + nbytes(t)].copy_(t.contiguous().view(-1).view(torch.uint8))
     outs_t = {"out": out, "lse": lse}
     out_offs, out_total = layout(outs_t)
-    d_in = [torch.empty(in_total, dtype=torch.uint8, device=dev) for _ in range(2)]
-    d_out = [torch.empty(out_total, dtype=torch.uint8, device=dev) for _ in range(2)]
-    h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d_in = [torch.empty(in_total, dtype=torch.uint8, device=dev) for _ in range(NB)]
+    d_out = [torch.empty(out_total, dtype=torch.uint8, device=dev) for _ in range(NB)]
+    h_out = [torch.empty(out_total, dtype=torch.uint8).pin_memory() for _ in range(NB)]
     sets = [views(b, host, in_offs) for b in d_in]
     outs = [(v["out"], v["lse"]) for v in (views(b, outs_t, out_offs) for b in d_out)]
     inp_bytes = sum(nbytes(v) for v in host.values())
     out_bytes = nbytes(out) + nbytes(lse)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    in_done = [torch.cuda.Event() for _ in range(args.steps)]
-    comp_done = [torch.cuda.Event() for _ in range(args.steps)]
-    out_done = [torch.cuda.Event() for _ in range(args.steps)]
+    groups = [(g0, min(g0 + G, args.steps)) for g0 in range(0, args.steps, G)]
+    in_done = [torch.cuda.Event() for _ in groups]
+    comp_done = [torch.cuda.Event() for _ in groups]
+    out_done = [torch.cuda.Event() for _ in groups]
     e2e_start, e2e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def copy_in(g):
+        # group g's inputs; its buffer sets were last used by group g - 2
+        with torch.cuda.stream(s_in):
+            if g >= 2:
+                s_in.wait_event(comp_done[g - 2])
+            for k in range(*groups[g]):
+                d_in[k % NB].copy_(h_in, non_blocking=True)
+            in_done[g].record(s_in)
+
     torch.cuda.synchronize()
     host_lead(stream)
     e2e_start.record(stream)
     s_in.wait_event(e2e_start)
-    for i in range(args.steps):
-        j = i & 1
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(comp_done[i - 2])          # buffer set j is free again
-            d_in[j].copy_(h_in, non_blocking=True)
-            in_done[i].record(s_in)
-        stream.wait_event(in_done[i])
-        if i >= 2:
-            stream.wait_event(out_done[i - 2])             # output set j has been read back
-        step(sets[j], *outs[j])
-        comp_done[i].record(stream)
+    copy_in(0)
+    for g, (k0, k1) in enumerate(groups):
+        if g + 1 < len(groups):
+            copy_in(g + 1)                                 # travels while group g computes
+        stream.wait_event(in_done[g])
+        if g >= 2:
+            stream.wait_event(out_done[g - 2])             # its output sets have been read back
+        for k in range(k0, k1):
+            step(sets[k % NB], *outs[k % NB])
+        comp_done[g].record(stream)
         with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[i])
-            h_out[j].copy_(d_out[j], non_blocking=True)
-            out_done[i].record(s_out)
-    stream.wait_event(out_done[args.steps - 1])
+            s_out.wait_event(comp_done[g])
+            for k in range(k0, k1):
+                h_out[k % NB].copy_(d_out[k % NB], non_blocking=True)
+            out_done[g].record(s_out)
+    stream.wait_event(out_done[-1])
     e2e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e2e_start.elapsed_time(e2e_end) / args.steps
@@ -423,8 +448,9 @@ def run_gpu(args):
             "l2": ("flushed (256 MiB write) before every timed step" if do_flush else
                    f"no flush: inputs larger than L2 -- each step reads {alg['kv'] / 1e6:.0f} MB of cache rows "
                    f"({alg['kv'] / L2_BYTES:.1f} x the 129 MB L2)"),
-            "timing": "value: K whole steps, CUDA events per step; roofline: a second pass of K steps "
-                      "with events around the decode kernel",
+            "timing": ("value: K whole steps, one CUDA event pair around them" if not do_flush else
+                       "value: K whole steps, CUDA events around each (the flush outside)")
+                      + "; roofline: a second pass of K steps with events around the decode kernel",
         },
         "hbm_gbs": round(achieved, 1),
         "tflops": round(achieved_tf, 1),
@@ -432,9 +458,9 @@ def run_gpu(args):
         "roofline": roof,
         "e2e": {"value": round(job_throughput(T, world, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": inp_bytes, "d2h_bytes_per_step": out_bytes,
-                "copies": "one packed pinned input buffer and one packed output buffer per step; step i+1's "
-                          "inputs and step i's outputs move on copy streams while step i computes (two device "
-                          "buffer sets)"},
+                "copies": f"one packed pinned input buffer and one packed output buffer per step; steps in "
+                          f"groups of {G}: group g+1's inputs and group g-1's outputs move on copy streams while "
+                          f"group g computes ({NB} device buffer sets)"},
         # per step: cache write, plan, decode, combine (+ two query quantisations with an e4m3 query)
         "gpu_launches": (6 if fp8q else 4) * args.steps,
         "clocks": clocks,
@@ -823,6 +849,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-requests", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-group", type=int, default=1,
+                    help="end-to-end leg: steps per group between the compute stream's waits for copies")
     ap.add_argument("--fp8-query", action="store_true",
                     help="e4m3 workloads: quantise the query each step and run the fp8 x fp8 decode")
     ap.add_argument("--op", default="decode", choices=["decode", "q_absorb", "v_up_proj", "gather"])
