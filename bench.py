@@ -373,26 +373,32 @@ def run_gpu(args):
                 d_in[k % NB].copy_(h_in, non_blocking=True)
             in_done[g].record(s_in)
 
+    def run_steps(cs, fork):
+        # every step's copies and kernels; `cs` is the compute stream, the copy
+        # streams start after `fork` (recorded on it) and rejoin it at the end
+        s_in.wait_event(fork)
+        s_out.wait_event(fork)
+        copy_in(0)
+        for g, (k0, k1) in enumerate(groups):
+            if g + 1 < len(groups):
+                copy_in(g + 1)                             # travels while group g computes
+            cs.wait_event(in_done[g])
+            if g >= 2:
+                cs.wait_event(out_done[g - 2])             # its output sets have been read back
+            for k in range(k0, k1):
+                step(sets[k % NB], *outs[k % NB])
+            comp_done[g].record(cs)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[g])
+                for k in range(k0, k1):
+                    h_out[k % NB].copy_(d_out[k % NB], non_blocking=True)
+                out_done[g].record(s_out)
+        cs.wait_event(out_done[-1])
+
     torch.cuda.synchronize()
     host_lead(stream)
     e2e_start.record(stream)
-    s_in.wait_event(e2e_start)
-    copy_in(0)
-    for g, (k0, k1) in enumerate(groups):
-        if g + 1 < len(groups):
-            copy_in(g + 1)                                 # travels while group g computes
-        stream.wait_event(in_done[g])
-        if g >= 2:
-            stream.wait_event(out_done[g - 2])             # its output sets have been read back
-        for k in range(k0, k1):
-            step(sets[k % NB], *outs[k % NB])
-        comp_done[g].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[g])
-            for k in range(k0, k1):
-                h_out[k % NB].copy_(d_out[k % NB], non_blocking=True)
-            out_done[g].record(s_out)
-    stream.wait_event(out_done[-1])
+    run_steps(stream, e2e_start)
     e2e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e2e_start.elapsed_time(e2e_end) / args.steps
