@@ -69,6 +69,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int (&sums)[2]
   return incl - v + before;
 }
 
+// floor(a / b) for 0 <= a < 2^24 and 0 < b < 2^24: a float estimate
+// corrected with integer products; an integer division is a long
+// chain of dependent instructions, and the plan is one chain of them.
+__device__ __forceinline__ int divf(int a, int b) {
+  int q = __float2int_rz(__fdividef((float)a, (float)b));
+  while (q * b > a) --q;          // the estimate is within a few units
+  while ((q + 1) * b <= a) ++q;
+  return q;
+}
+
 // floor(a * b / c) for a, b >= 0 and c > 0: a 32-bit division whenever the
 // product fits (a 64-bit division is a long chain of dependent instructions)
 __device__ __forceinline__ int muldiv(int a, int b, int c) {
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         r.b = b;
         r.row0 = q0 * N + g * GR;
         r.nrows = min(GR, rows_b - g * GR);
-        const int t_last = (g * GR + r.nrows - 1) / N;
+        const int t_last = divf(g * GR + r.nrows - 1, N);
         long long L = seq - sq + 1 + t_last;
         if (L < 0) L = 0;
         if (L > kv_cap) L = kv_cap;
@@ -172,13 +182,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     carry += total;
   }
   const int T = carry;
-  const int W = T > 0 ? (T + C - 1) / C : 1;
   // Span c of the axis is [floor(c T / Cs), floor((c+1) T / Cs)) with
-  // Cs = min(C, T) spans, none of them empty.  The span starts are computed
-  // once (one division per thread); the span of a position is a float
-  // estimate corrected against them.
+  // Cs = min(C, T) spans, none of them empty.  With T = a Cs + b, the start
+  // of span c is c a + floor(c b / Cs) (c b < Cs^2: a short division); the
+  // span of a position is a float estimate corrected against the starts.
   const int Cs = T < C ? (T > 0 ? T : 1) : C;
-  for (int c = tid; c <= Cs; c += kPlanThreads) s_span[c] = muldiv(c, T, Cs);
+  const bool small_axis = T < (1 << 24);
+  const int sa = small_axis ? divf(T, Cs) : T / Cs;
+  const int sb = T - sa * Cs;
+  const int W = T > 0 ? (T >= C ? sa + (sb > 0) : 1) : 1;   // ceil(T / C) positions per span
+  for (int c = tid; c <= Cs; c += kPlanThreads) s_span[c] = c * sa + divf(c * sb, Cs);
   const float span_per_pos = T > 0 ? __fdividef((float)Cs, (float)T) : 0.f;
   auto span_start = [&](int c) { return s_span[c]; };
   auto span_of = [&](int p) {
@@ -201,7 +214,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         if (num_splits > 0)
           pieces = min(num_splits, r.tiles);
         else
-          pieces = span_of(s0 + r.tiles - 1) - span_of(s0) + 1;
+          pieces = span_of(s0 + r.tiles - 1) - span_of(s0) + 1;   // spans the group's real tiles touch
       }
     }
     int total;
@@ -234,6 +247,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
       const long long seq = min((long long)seq_lens[r.b], kv_cap);
       kbase = (int)(seq - sq + 1 - q0);
     }
+    const int c0 = num_splits > 0 || r.pieces == 0 ? 0 : span_of(s0);   // the span of the group's first piece
     for (int i = 0; i < r.pieces; ++i) {
       UnitRec u;
       int cl;
@@ -247,7 +261,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
         u.tile_end = muldiv(i + 1, r.tiles, r.pieces);
         cl = min(C - 1, span_of(s0 + (u.tile_begin + u.tile_end) / 2));
       } else {
-        cl = span_of(s0) + i;
+        cl = c0 + i;
         u.tile_begin = max(s0, span_start(cl)) - s0;
         u.tile_end = min(s0 + r.tiles, span_start(cl + 1)) - s0;
       }
