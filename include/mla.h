@@ -153,6 +153,23 @@ MLA_API int mla_decode(const void* q_abs, const void* q_pe, const void* cache, i
                size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_step -- one decode step: mla_cache_write of the step's new rows
+ * (kv_c [num_new_tokens, 512] bf16, k_pe [num_new_tokens, 64] bf16 into the
+ * slots slot_mapping [num_new_tokens] int64, a negative slot is padding),
+ * then mla_decode over the updated cache: the same results as the two calls
+ * in that order, with the same argument rules.  The rows are written by
+ * extra blocks of the scheduler's launch, which run beside the split plan,
+ * so the write costs the step no launch of its own.  num_new_tokens == 0
+ * writes nothing; batch == 0 or total_q == 0 only writes.
+ */
+MLA_API int mla_decode_step(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_new_tokens,
+                            const void* q_abs, const void* q_pe, void* cache, int64_t num_blocks, int page_size,
+                            int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+                            const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q,
+                            int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * mla_decode_status -- copy the device error word of the last mla_decode that
  * used `workspace` (OR of mla_device_error bits; 0 = clean) to *status.
  * Synchronises `stream`.  The word is cleared by every mla_decode.

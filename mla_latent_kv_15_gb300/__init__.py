@@ -30,7 +30,7 @@ C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
                  "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
                  "mla_gather_cache", "mla_quantize_fp8", "mla_decode_fp8q", "mla_set_decode_wait_test",
-                 "mla_decode_no_alloc_status")
+                 "mla_decode_no_alloc_status", "mla_decode_step")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -85,6 +85,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_set_decode_wait_test.argtypes = [i32, ctypes.c_ulonglong]
     lib.mla_decode_no_alloc_status.restype = i32
     lib.mla_decode_no_alloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
+    lib.mla_decode_step.restype = i32
+    lib.mla_decode_step.argtypes = [P, P, P, i64, P, P, P, i64, i32, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32,
+                                    P, P, P, sz, P]
     _lib = lib
     return lib
 
@@ -177,6 +180,27 @@ def decode(q_abs, q_pe, cache, block_table, seq_lens, out, workspace, *, scale: 
                              _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc),
                              T, N, float(scale), int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_step(kv_c, k_pe, slot_mapping, q_abs, q_pe, cache, block_table, seq_lens, out, workspace, *,
+                scale: float, query_start_loc=None, lse=None, num_splits: int = 0, kv_scale: float = 1.0,
+                stream=None) -> None:
+    """cache_write(kv_c, k_pe, slot_mapping, cache) then decode(...) in one
+    call: the new rows are written by extra blocks of the scheduler's launch."""
+    import torch
+    T, N, _ = q_abs.shape
+    nb, ps, _ = _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse)
+    _dense(slot_mapping, "slot_mapping", torch.int64, dims=1)
+    W = slot_mapping.numel()
+    _dense(kv_c, "kv_c", torch.bfloat16, (W, LKV))
+    _dense(k_pe, "k_pe", torch.bfloat16, (W, ROPE))
+    _dense(workspace, "workspace", (workspace.dtype,))
+    B = seq_lens.numel()
+    _check(load().mla_decode_step(_ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), W, _ptr(q_abs), _ptr(q_pe),
+                                  _ptr(cache), nb, ps, _dtype_code(cache), float(kv_scale), _ptr(block_table),
+                                  block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc), T, N, float(scale),
+                                  int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse, q8=None):

@@ -58,6 +58,30 @@ namespace mla {
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 }  // namespace mla
 
+namespace {
+
+// Checks of a cache write's arguments (mla_cache_write, mla_decode_step);
+// fills *w when they pass (num_tokens == 0 passes and writes nothing).
+int cache_write_args(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_tokens, void* cache,
+                     int64_t num_blocks, int page_size, int cache_dtype, float kv_scale, mla::CacheWriteArgs* w) {
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)num_tokens);
+  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3)
+    return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
+  if (page_size <= 0 || num_blocks <= 0)
+    return fail(MLA_ERR_INVALID_ARG, "page_size and num_blocks must be positive");
+  if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
+    return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
+  *w = mla::CacheWriteArgs{kv_c, k_pe, slot_mapping, num_tokens, cache, num_blocks * page_size, kv_scale,
+                           cache_dtype == MLA_FP8_E4M3};
+  if (num_tokens == 0) return ok();
+  if (!kv_c || !k_pe || !slot_mapping || !cache) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
+    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe and cache must be 16-byte aligned, slot_mapping 8-byte aligned");
+  return ok();
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* mla_last_error(void) { return g_last_error.c_str(); }
@@ -86,19 +110,11 @@ int mla_device_sm_count(void) {
 int mla_cache_write(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_tokens,
                     void* cache, int64_t num_blocks, int page_size, int cache_dtype, float kv_scale,
                     void* stream) {
-  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %lld)", (long long)num_tokens);
-  if (cache_dtype != MLA_BF16 && cache_dtype != MLA_FP8_E4M3)
-    return fail(MLA_ERR_INVALID_ARG, "cache_dtype must be MLA_BF16 or MLA_FP8_E4M3 (got %d)", cache_dtype);
-  if (page_size <= 0 || num_blocks <= 0)
-    return fail(MLA_ERR_INVALID_ARG, "page_size and num_blocks must be positive");
-  if (cache_dtype == MLA_FP8_E4M3 && !(std::isfinite(kv_scale) && kv_scale > 0.f))
-    return fail(MLA_ERR_INVALID_ARG, "kv_scale must be finite and > 0 for an fp8 cache");
-  if (num_tokens == 0) return ok();
-  if (!kv_c || !k_pe || !slot_mapping || !cache) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
-  if (!aligned(kv_c, 16) || !aligned(k_pe, 16) || !aligned(cache, 16) || !aligned(slot_mapping, 8))
-    return fail(MLA_ERR_INVALID_ARG, "kv_c, k_pe and cache must be 16-byte aligned, slot_mapping 8-byte aligned");
-  cudaError_t e = mla::launch_cache_write(kv_c, k_pe, slot_mapping, num_tokens, cache, num_blocks * page_size,
-                                          cache_dtype == MLA_FP8_E4M3, kv_scale, (cudaStream_t)stream);
+  mla::CacheWriteArgs w;
+  const int rc = cache_write_args(kv_c, k_pe, slot_mapping, num_tokens, cache, num_blocks, page_size, cache_dtype,
+                                  kv_scale, &w);
+  if (rc != MLA_OK || num_tokens == 0) return rc;
+  cudaError_t e = mla::launch_cache_write(w, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cache write launch");
   return ok();
 }
@@ -118,7 +134,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
                 int64_t num_blocks, int page_size, int cache_dtype, float kv_scale, const int32_t* block_table,
                 int max_pages_per_seq, const int32_t* seq_lens, int batch, const int32_t* query_start_loc,
                 int total_q, int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream) {
+                size_t workspace_bytes, void* stream, const mla::CacheWriteArgs* write = nullptr) {
   if (batch < 0 || total_q < 0) return fail(MLA_ERR_INVALID_ARG, "batch and total_q must be >= 0");
   if (num_heads < 1 || num_heads > 1024) return fail(MLA_ERR_INVALID_ARG, "num_heads must be in [1, 1024]");
   if (batch == 0 || total_q == 0) return ok();
@@ -236,7 +252,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   const int small_rows = !q8 && cache_dtype == MLA_BF16 && num_heads <= 32 && total_q == batch;
   const int variant = q8 ? 3 : (cache_dtype == MLA_FP8_E4M3 ? 1 : (small_rows ? 2 : 0));
   cudaError_t e = mla::launch_plan(seq_lens, query_start_loc, batch, num_heads, max_pages_per_seq, page_size,
-                                   num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, s);
+                                   num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, write, s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
@@ -260,6 +276,24 @@ int mla_decode(const void* q_abs, const void* q_pe, const void* cache, int64_t n
   return decode_impl(q_abs, q_pe, nullptr, 0.f, cache, num_blocks, page_size, cache_dtype, kv_scale, block_table,
                      max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale, num_splits, out,
                      lse, workspace, workspace_bytes, stream);
+}
+
+int mla_decode_step(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_new_tokens,
+                    const void* q_abs, const void* q_pe, void* cache, int64_t num_blocks, int page_size,
+                    int cache_dtype, float kv_scale, const int32_t* block_table, int max_pages_per_seq,
+                    const int32_t* seq_lens, int batch, const int32_t* query_start_loc, int total_q, int num_heads,
+                    float scale, int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  mla::CacheWriteArgs w;
+  const int rc = cache_write_args(kv_c, k_pe, slot_mapping, num_new_tokens, cache, num_blocks, page_size,
+                                  cache_dtype, kv_scale, &w);
+  if (rc != MLA_OK) return rc;
+  if (batch == 0 || total_q == 0)   // no decode: the write alone
+    return mla_cache_write(kv_c, k_pe, slot_mapping, num_new_tokens, cache, num_blocks, page_size, cache_dtype,
+                           kv_scale, stream);
+  return decode_impl(q_abs, q_pe, nullptr, 0.f, cache, num_blocks, page_size, cache_dtype, kv_scale, block_table,
+                     max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale, num_splits, out,
+                     lse, workspace, workspace_bytes, stream, num_new_tokens > 0 ? &w : nullptr);
 }
 
 int mla_decode_fp8q(const void* q_fp8, float q_scale, const void* cache, int64_t num_blocks, int page_size,

@@ -136,10 +136,27 @@ struct DecodeArgs {
   Plan plan;
 };
 
+// The new rows of a step for concat_and_cache_mla: token t's kv_c (512 bf16)
+// and k_pe (64 bf16) go to cache slot slots[t] (a slot outside
+// [0, num_slots) is padding); an e4m3 cache stores value / kv_scale.
+struct CacheWriteArgs {
+  const void* kv_c;
+  const void* k_pe;
+  const int64_t* slots;
+  int64_t num_tokens;
+  void* cache;
+  int64_t num_slots;
+  float kv_scale;
+  int fp8;
+};
+
 // ---- launchers (return cudaError_t of the launch)
 // group_rows: query rows per group, a power of two (128; 32 for the small-rows decode variant)
+// write: the step's cache rows, written by extra blocks of the same launch
+// (nullptr: none)
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
-                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s);
+                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan,
+                        const CacheWriteArgs* write, cudaStream_t s);
 // variant: 0 bf16 cache, 1 e4m3 cache, 2 bf16 cache with <= 32-row groups
 // (plan built with group_rows = 32), 3 e4m3 query and e4m3 cache.  Tensor
 // maps: the query's latent columns (64-dim boxes; 128-dim e4m3 boxes for
@@ -154,8 +171,7 @@ cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cu
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                                 int64_t rows, int dim, int o_is_bf16, void* out, float* lse_out, int sm_count,
                                 cudaStream_t s);
-cudaError_t launch_cache_write(const void* kv_c, const void* k_pe, const int64_t* slots, int64_t num_tokens,
-                               void* cache, int64_t num_slots, int cache_fp8, float kv_scale, cudaStream_t s);
+cudaError_t launch_cache_write(const CacheWriteArgs& w, cudaStream_t s);
 size_t decode_smem_bytes(int variant);
 // y[t, n, :] = x[t, n, :] @ W[n] (tensor maps: x 3-D {d_in, N, T} boxes
 // 64 x 1 x head_proj_x_rows(T), W 2-D {d_out, N*d_in} boxes 64x64, both

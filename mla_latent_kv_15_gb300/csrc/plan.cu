@@ -16,6 +16,7 @@
 //     pieces and pieces go to the pair whose span holds their midpoint.
 // Pieces of a split group write partials that the combine kernel merges
 // with the LSE rule of merge_attn_states.
+#include "cache_rows.cuh"
 #include "common.cuh"
 
 namespace mla {
@@ -90,11 +91,25 @@ __device__ __forceinline__ int muldiv(int a, int b, int c) {
 // kStaged: the group records and unit clusters live in shared memory while
 // the plan is built (each phase reads what other threads wrote in the
 // previous one) and are copied out at the end; for plans that fit.
-template <bool kStaged>
+// kWrite (1 bf16, 2 e4m3 cache): blocks 1.. of the launch write the step's
+// new cache rows (8 tokens a block) while block 0 builds the plan, so the
+// cache write costs the step no launch of its own.
+template <bool kStaged, int kWrite>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ qsl, int batch, int N,
                                                     int max_pages, int page_size, int num_splits, int C,
-                                                    int GR, Plan P) {
+                                                    int GR, Plan P, const CacheWriteArgs w) {
+  if constexpr (kWrite != 0) {
+    if (blockIdx.x > 0) {
+      // as the cache-write kernel: wait for the kernel before, then let the
+      // next one launch (the decode waits for this whole grid)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      const int64_t tok = (blockIdx.x - 1) * 8LL + (threadIdx.x >> 5);
+      if (tok < w.num_tokens) write_cache_row<kWrite == 2>(w, tok, threadIdx.x & 31);
+      return;
+    }
+  }
   __shared__ int s_flags;
   __shared__ int s_span[kMaxClusters + 1];   // first axis position of every span
   __shared__ GroupRec s_groups[kStaged ? kPlanSmemGroups : 1];
@@ -299,9 +314,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
-                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan, cudaStream_t s) {
+                        int page_size, int num_splits, int num_clusters, int group_rows, Plan plan,
+                        const CacheWriteArgs* write, cudaStream_t s) {
+  const bool writes = write && write->num_tokens > 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
+  cfg.gridDim = dim3(1 + (writes ? (unsigned)((write->num_tokens + 7) / 8) : 0u));
   cfg.blockDim = dim3(kPlanThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -310,8 +327,13 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool staged = plan.max_groups <= kPlanSmemGroups && plan.max_units <= kPlanSmemUnits;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, staged ? plan_kernel<true> : plan_kernel<false>, seq_lens, qsl, batch,
-                                     num_heads, max_pages, page_size, num_splits, num_clusters, group_rows, plan);
+  const int mode = writes ? (write->fp8 ? 2 : 1) : 0;
+  const CacheWriteArgs w = writes ? *write : CacheWriteArgs{};
+  using Kernel = void (*)(const int32_t*, const int32_t*, int, int, int, int, int, int, int, Plan, const CacheWriteArgs);
+  static const Kernel kernels[2][3] = {{plan_kernel<false, 0>, plan_kernel<false, 1>, plan_kernel<false, 2>},
+                                       {plan_kernel<true, 0>, plan_kernel<true, 1>, plan_kernel<true, 2>}};
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernels[staged][mode], seq_lens, qsl, batch, num_heads, max_pages,
+                                     page_size, num_splits, num_clusters, group_rows, plan, w);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
