@@ -252,12 +252,13 @@ def run_gpu(args):
                             inp["block_table"], inp["seq_lens"], o, ws, scale=case.scale, query_start_loc=inp["qsl"],
                             lse=lo, num_splits=args.num_splits, kv_scale=case.kv_scale)
             return
-        mla.cache_write(inp["kv_c"], inp["k_pe"], inp["slots"], cache, case.kv_scale)
-        # scaled_fp8_quant of q_abs and q_pe into [q_abs | q_pe] rows, then the fp8 x fp8 decode
-        mla.quantize_fp8(inp["q_abs"], q_scale, q8[..., :synth.LKV])
-        mla.quantize_fp8(inp["q_pe"], q_scale, q8[..., synth.LKV:])
-        mla.decode_fp8q(q8, q_scale, cache, inp["block_table"], inp["seq_lens"], o, ws, scale=case.scale,
-                        query_start_loc=inp["qsl"], lse=lo, num_splits=args.num_splits, kv_scale=case.kv_scale)
+        # the cache write, scaled_fp8_quant of q_abs and q_pe into [q_abs | q_pe]
+        # rows (both by extra blocks of the scheduler's launch) and the fp8 x
+        # fp8 decode in one call
+        mla.decode_fp8q_step(inp["kv_c"], inp["k_pe"], inp["slots"], inp["q_abs"], inp["q_pe"], q_scale, q8, cache,
+                             inp["block_table"], inp["seq_lens"], o, ws, scale=case.scale,
+                             query_start_loc=inp["qsl"], lse=lo, num_splits=args.num_splits,
+                             kv_scale=case.kv_scale)
 
     for _ in range(args.warmup):
         step(d)
@@ -469,9 +470,9 @@ def run_gpu(args):
                 "copies": f"one packed pinned input buffer and one packed output buffer per step; steps in "
                           f"groups of {G}: group g+1's inputs and group g-1's outputs move on copy streams while "
                           f"group g computes ({NB} device buffer sets)"},
-        # per step: plan (with the cache write), decode, combine; with an e4m3
-        # query: cache write, two query quantisations, plan, decode, combine
-        "gpu_launches": (6 if fp8q else 3) * args.steps,
+        # per step: plan (with the cache write, and with an e4m3 query its
+        # quantisation), decode, combine
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

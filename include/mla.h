@@ -329,6 +329,25 @@ MLA_API int mla_decode_fp8q(const void* q_fp8, float q_scale, const void* cache,
                             size_t workspace_bytes, void* stream);
 
 /*
+ * mla_decode_fp8q_step -- one e4m3-query step: mla_cache_write of the step's
+ * new rows into the e4m3 cache, mla_quantize_fp8 of q_abs [total_q,
+ * num_heads, 512] and q_pe [total_q, num_heads, 64] (bf16, dense) with
+ * q_scale into q_fp8 [total_q, num_heads, 576] (e4m3 codes of [q_abs | q_pe],
+ * written by this call), then mla_decode_fp8q: the same results as those
+ * calls in that order, with the same argument rules.  The cache rows and the
+ * query codes are written by extra blocks of the scheduler's launch, beside
+ * the split plan.  num_new_tokens == 0 writes no cache row; batch == 0 or
+ * total_q == 0 only writes the cache rows.
+ */
+MLA_API int mla_decode_fp8q_step(const void* kv_c, const void* k_pe, const int64_t* slot_mapping,
+                                 int64_t num_new_tokens, const void* q_abs, const void* q_pe, float q_scale,
+                                 void* q_fp8, void* cache, int64_t num_blocks, int page_size, float kv_scale,
+                                 const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                 int batch, const int32_t* query_start_loc, int total_q, int num_heads, float scale,
+                                 int num_splits, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
  * mla_quantize_fp8 -- scaled_fp8_quant with a static per-tensor scale, as the
  * decode branch applies it to the absorbed query and q_pe when the cache is
  * fp8 (common.py, MLACommonImpl.forward: scaled_fp8_quant(..., layer._q_scale)):

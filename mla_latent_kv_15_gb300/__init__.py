@@ -30,7 +30,7 @@ C_ABI_SYMBOLS = ("mla_cache_write", "mla_decode_workspace_size", "mla_decode", "
                  "mla_merge_states", "mla_last_error", "mla_device_sm_count", "mla_set_decode_timing_events",
                  "mla_decode_no_alloc", "mla_q_absorb", "mla_v_up_proj", "mla_proj_status",
                  "mla_gather_cache", "mla_quantize_fp8", "mla_decode_fp8q", "mla_set_decode_wait_test",
-                 "mla_decode_no_alloc_status", "mla_decode_step")
+                 "mla_decode_no_alloc_status", "mla_decode_step", "mla_decode_fp8q_step")
 NO_ALLOC_SCRATCH_BYTES = 96 << 20
 
 _lib = None
@@ -85,6 +85,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_set_decode_wait_test.argtypes = [i32, ctypes.c_ulonglong]
     lib.mla_decode_no_alloc_status.restype = i32
     lib.mla_decode_no_alloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), i32, P]
+    lib.mla_decode_fp8q_step.restype = i32
+    lib.mla_decode_fp8q_step.argtypes = [P, P, P, i64, P, P, f32, P, P, i64, i32, f32, P, i32, P, i32, P, i32, i32, f32,
+                                         i32, P, P, P, sz, P]
     lib.mla_decode_step.restype = i32
     lib.mla_decode_step.argtypes = [P, P, P, i64, P, P, P, i64, i32, i32, f32, P, i32, P, i32, P, i32, i32, f32, i32,
                                     P, P, P, sz, P]
@@ -201,6 +204,34 @@ def decode_step(kv_c, k_pe, slot_mapping, q_abs, q_pe, cache, block_table, seq_l
                                   block_table.shape[1], _ptr(seq_lens), B, _ptr(query_start_loc), T, N, float(scale),
                                   int(num_splits), _ptr(out), _ptr(lse), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def decode_fp8q_step(kv_c, k_pe, slot_mapping, q_abs, q_pe, q_scale: float, q_fp8, cache, block_table, seq_lens,
+                     out, workspace, *, scale: float, query_start_loc=None, lse=None, num_splits: int = 0,
+                     kv_scale: float = 1.0, stream=None) -> None:
+    """cache_write, quantize_fp8 of q_abs and q_pe into ``q_fp8`` [T, N, 576]
+    ([q_abs | q_pe] e4m3 rows, written by this call) and decode_fp8q in one
+    call: the rows and the codes are written by extra blocks of the
+    scheduler's launch."""
+    import torch
+    _dense(q_abs, "q_abs", torch.bfloat16, (None, None, LKV))
+    T, N, _ = q_abs.shape
+    _dense(q_pe, "q_pe", torch.bfloat16, (T, N, ROPE))
+    nb, ps, _ = _decode_checked(None, None, cache, block_table, seq_lens, out, query_start_loc, lse, q8=q_fp8)
+    if tuple(q_fp8.shape[:2]) != (T, N):
+        raise ValueError(f"q_fp8 must have shape [{T}, {N}, {DQK}], got {tuple(q_fp8.shape)}")
+    _dense(slot_mapping, "slot_mapping", torch.int64, dims=1)
+    W = slot_mapping.numel()
+    _dense(kv_c, "kv_c", torch.bfloat16, (W, LKV))
+    _dense(k_pe, "k_pe", torch.bfloat16, (W, ROPE))
+    _dense(workspace, "workspace", (workspace.dtype,))
+    B = seq_lens.numel()
+    _check(load().mla_decode_fp8q_step(_ptr(kv_c), _ptr(k_pe), _ptr(slot_mapping), W, _ptr(q_abs), _ptr(q_pe),
+                                       float(q_scale), _ptr(q_fp8), _ptr(cache), nb, ps, float(kv_scale),
+                                       _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                       _ptr(query_start_loc), T, N, float(scale), int(num_splits), _ptr(out),
+                                       _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
 
 
 def _decode_checked(q_abs, q_pe, cache, block_table, seq_lens, out, query_start_loc, lse, q8=None):

@@ -134,7 +134,8 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
                 int64_t num_blocks, int page_size, int cache_dtype, float kv_scale, const int32_t* block_table,
                 int max_pages_per_seq, const int32_t* seq_lens, int batch, const int32_t* query_start_loc,
                 int total_q, int num_heads, float scale, int num_splits, void* out, float* lse, void* workspace,
-                size_t workspace_bytes, void* stream, const mla::CacheWriteArgs* write = nullptr) {
+                size_t workspace_bytes, void* stream, const mla::CacheWriteArgs* write = nullptr,
+                const mla::QuantArgs* quant = nullptr) {
   if (batch < 0 || total_q < 0) return fail(MLA_ERR_INVALID_ARG, "batch and total_q must be >= 0");
   if (num_heads < 1 || num_heads > 1024) return fail(MLA_ERR_INVALID_ARG, "num_heads must be in [1, 1024]");
   if (batch == 0 || total_q == 0) return ok();
@@ -252,7 +253,8 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   const int small_rows = !q8 && cache_dtype == MLA_BF16 && num_heads <= 32 && total_q == batch;
   const int variant = q8 ? 3 : (cache_dtype == MLA_FP8_E4M3 ? 1 : (small_rows ? 2 : 0));
   cudaError_t e = mla::launch_plan(seq_lens, query_start_loc, batch, num_heads, max_pages_per_seq, page_size,
-                                   num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, write, s);
+                                   num_splits, clusters, small_rows ? 32 : mla::kRows, a.plan, write, quant, sms,
+                                   s);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
@@ -294,6 +296,32 @@ int mla_decode_step(const void* kv_c, const void* k_pe, const int64_t* slot_mapp
   return decode_impl(q_abs, q_pe, nullptr, 0.f, cache, num_blocks, page_size, cache_dtype, kv_scale, block_table,
                      max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale, num_splits, out,
                      lse, workspace, workspace_bytes, stream, num_new_tokens > 0 ? &w : nullptr);
+}
+
+int mla_decode_fp8q_step(const void* kv_c, const void* k_pe, const int64_t* slot_mapping, int64_t num_new_tokens,
+                         const void* q_abs, const void* q_pe, float q_scale, void* q_fp8, void* cache,
+                         int64_t num_blocks, int page_size, float kv_scale, const int32_t* block_table,
+                         int max_pages_per_seq, const int32_t* seq_lens, int batch, const int32_t* query_start_loc,
+                         int total_q, int num_heads, float scale, int num_splits, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  mla::CacheWriteArgs w;
+  int rc = cache_write_args(kv_c, k_pe, slot_mapping, num_new_tokens, cache, num_blocks, page_size, MLA_FP8_E4M3,
+                            kv_scale, &w);
+  if (rc != MLA_OK) return rc;
+  if (batch == 0 || total_q == 0)   // no decode: the write alone
+    return mla_cache_write(kv_c, k_pe, slot_mapping, num_new_tokens, cache, num_blocks, page_size, MLA_FP8_E4M3,
+                           kv_scale, stream);
+  if (!q_abs || !q_pe || !q_fp8) return fail(MLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned(q_abs, 16) || !aligned(q_pe, 16) || !aligned(q_fp8, 16))
+    return fail(MLA_ERR_INVALID_ARG, "q_abs, q_pe and q_fp8 must be 16-byte aligned");
+  if (!(std::isfinite(q_scale) && q_scale > 0.f)) return fail(MLA_ERR_INVALID_ARG, "q_scale must be finite and > 0");
+  if (total_q < 0 || num_heads < 1 || num_heads > 1024)
+    return fail(MLA_ERR_INVALID_ARG, "total_q must be >= 0 and num_heads in [1, 1024]");
+  const mla::QuantArgs qa{q_abs, q_pe, (int64_t)total_q * num_heads, q_scale, static_cast<uint8_t*>(q_fp8)};
+  return decode_impl(nullptr, nullptr, q_fp8, q_scale, cache, num_blocks, page_size, MLA_FP8_E4M3, kv_scale,
+                     block_table, max_pages_per_seq, seq_lens, batch, query_start_loc, total_q, num_heads, scale,
+                     num_splits, out, lse, workspace, workspace_bytes, stream, num_new_tokens > 0 ? &w : nullptr,
+                     &qa);
 }
 
 int mla_decode_fp8q(const void* q_fp8, float q_scale, const void* cache, int64_t num_blocks, int page_size,

@@ -1,5 +1,5 @@
-// concat_and_cache_mla (the row write itself is in cache_rows.cuh) and
-// scaled_fp8_quant.
+// concat_and_cache_mla and scaled_fp8_quant kernels (the row write and the
+// eight-value quantisation themselves are in cache_rows.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -35,19 +35,8 @@ __global__ void __launch_bounds__(256) quantize_fp8_kernel(const __nv_bfloat16* 
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = v / vpr;
     const int c = (int)(v - r * vpr) * 8;
-    const uint4 src = *reinterpret_cast<const uint4*>(x + r * x_stride + c);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&src);
-    float lo[4], hi[4];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 f0 = __bfloat1622float2(h[k]);
-      const float2 f1 = __bfloat1622float2(h[2 + k]);
-      lo[2 * k] = __fdiv_rn(f0.x, scale);
-      lo[2 * k + 1] = __fdiv_rn(f0.y, scale);
-      hi[2 * k] = __fdiv_rn(f1.x, scale);
-      hi[2 * k + 1] = __fdiv_rn(f1.y, scale);
-    }
-    *reinterpret_cast<uint2*>(out + r * out_stride + c) = make_uint2(fp8x4(lo), fp8x4(hi));
+    *reinterpret_cast<uint2*>(out + r * out_stride + c) =
+        quantize8(*reinterpret_cast<const uint4*>(x + r * x_stride + c), scale);
   }
 }
 

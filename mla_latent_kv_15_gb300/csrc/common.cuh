@@ -150,13 +150,25 @@ struct CacheWriteArgs {
   int fp8;
 };
 
+// The query of an e4m3-query step: q_abs [rows, 512] and q_pe [rows, 64] bf16
+// (rows = total_q * num_heads, dense) into q8 [rows, 576] e4m3 codes of
+// value / q_scale.
+struct QuantArgs {
+  const void* q_abs;
+  const void* q_pe;
+  int64_t rows;
+  float q_scale;
+  uint8_t* q8;
+};
+
 // ---- launchers (return cudaError_t of the launch)
 // group_rows: query rows per group, a power of two (128; 32 for the small-rows decode variant)
-// write: the step's cache rows, written by extra blocks of the same launch
-// (nullptr: none)
+// write: the step's cache rows, quant: the step's query quantisation, both
+// done by extra blocks of the same launch (nullptr: none; quant needs an
+// e4m3 cache write or none)
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan,
-                        const CacheWriteArgs* write, cudaStream_t s);
+                        const CacheWriteArgs* write, const QuantArgs* quant, int sm_count, cudaStream_t s);
 // variant: 0 bf16 cache, 1 e4m3 cache, 2 bf16 cache with <= 32-row groups
 // (plan built with group_rows = 32), 3 e4m3 query and e4m3 cache.  Tensor
 // maps: the query's latent columns (64-dim boxes; 128-dim e4m3 boxes for

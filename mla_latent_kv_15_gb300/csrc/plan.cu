@@ -91,22 +91,35 @@ __device__ __forceinline__ int muldiv(int a, int b, int c) {
 // kStaged: the group records and unit clusters live in shared memory while
 // the plan is built (each phase reads what other threads wrote in the
 // previous one) and are copied out at the end; for plans that fit.
-// kWrite (1 bf16, 2 e4m3 cache): blocks 1.. of the launch write the step's
-// new cache rows (8 tokens a block) while block 0 builds the plan, so the
-// cache write costs the step no launch of its own.
-template <bool kStaged, int kWrite>
+// kMode: blocks 1.. of the launch do the step's other small jobs while block
+// 0 builds the plan, so they cost the step no launch of their own: the new
+// cache rows (blocks 1 .. write_blocks, 8 tokens a block; 1 bf16 cache,
+// 2 e4m3 cache) and, in mode 3 (e4m3 cache), the query's quantisation (the
+// remaining blocks, grid-stride over its 8-value vectors).
+template <bool kStaged, int kMode>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ seq_lens,
                                                     const int32_t* __restrict__ qsl, int batch, int N,
                                                     int max_pages, int page_size, int num_splits, int C,
-                                                    int GR, Plan P, const CacheWriteArgs w) {
-  if constexpr (kWrite != 0) {
+                                                    int GR, Plan P, const CacheWriteArgs w, const QuantArgs qa,
+                                                    int write_blocks) {
+  if constexpr (kMode != 0) {
     if (blockIdx.x > 0) {
       // as the cache-write kernel: wait for the kernel before, then let the
       // next one launch (the decode waits for this whole grid)
       asm volatile("griddepcontrol.wait;" ::: "memory");
       asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-      const int64_t tok = (blockIdx.x - 1) * 8LL + (threadIdx.x >> 5);
-      if (tok < w.num_tokens) write_cache_row<kWrite == 2>(w, tok, threadIdx.x & 31);
+      const int b = (int)blockIdx.x - 1;
+      if (b < write_blocks) {
+        const int64_t tok = b * 8LL + (threadIdx.x >> 5);
+        if (tok < w.num_tokens) write_cache_row<kMode >= 2>(w, tok, threadIdx.x & 31);
+        return;
+      }
+      if constexpr (kMode == 3) {
+        const int64_t nvec = qa.rows * (kDqk / 8);
+        const int64_t stride = (int64_t)(gridDim.x - 1 - write_blocks) * kPlanThreads;
+        for (int64_t v = (int64_t)(b - write_blocks) * kPlanThreads + threadIdx.x; v < nvec; v += stride)
+          quantize_query_vec(qa, v);
+      }
       return;
     }
   }
@@ -315,10 +328,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 
 cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, int num_heads, int max_pages,
                         int page_size, int num_splits, int num_clusters, int group_rows, Plan plan,
-                        const CacheWriteArgs* write, cudaStream_t s) {
+                        const CacheWriteArgs* write, const QuantArgs* quant, int sm_count, cudaStream_t s) {
   const bool writes = write && write->num_tokens > 0;
+  const int write_blocks = writes ? (int)((write->num_tokens + 7) / 8) : 0;
+  int quant_blocks = 0;
+  if (quant) {
+    // grid-stride: at most two blocks per SM (each holds the plan's shared memory)
+    const int64_t want = (quant->rows * (kDqk / 8) + kPlanThreads - 1) / kPlanThreads;
+    const int64_t cap = 2LL * (sm_count > 0 ? sm_count : 1);
+    quant_blocks = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1 + (writes ? (unsigned)((write->num_tokens + 7) / 8) : 0u));
+  cfg.gridDim = dim3(1u + (unsigned)write_blocks + (unsigned)quant_blocks);
   cfg.blockDim = dim3(kPlanThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -327,13 +348,17 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool staged = plan.max_groups <= kPlanSmemGroups && plan.max_units <= kPlanSmemUnits;
-  const int mode = writes ? (write->fp8 ? 2 : 1) : 0;
+  const int mode = quant ? 3 : (writes ? (write->fp8 ? 2 : 1) : 0);
+  if (quant && writes && !write->fp8) return cudaErrorInvalidValue;   // an e4m3 query goes with an e4m3 cache
   const CacheWriteArgs w = writes ? *write : CacheWriteArgs{};
-  using Kernel = void (*)(const int32_t*, const int32_t*, int, int, int, int, int, int, int, Plan, const CacheWriteArgs);
-  static const Kernel kernels[2][3] = {{plan_kernel<false, 0>, plan_kernel<false, 1>, plan_kernel<false, 2>},
-                                       {plan_kernel<true, 0>, plan_kernel<true, 1>, plan_kernel<true, 2>}};
+  const QuantArgs qa = quant ? *quant : QuantArgs{};
+  using Kernel = void (*)(const int32_t*, const int32_t*, int, int, int, int, int, int, int, Plan,
+                          const CacheWriteArgs, const QuantArgs, int);
+  static const Kernel kernels[2][4] = {
+      {plan_kernel<false, 0>, plan_kernel<false, 1>, plan_kernel<false, 2>, plan_kernel<false, 3>},
+      {plan_kernel<true, 0>, plan_kernel<true, 1>, plan_kernel<true, 2>, plan_kernel<true, 3>}};
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernels[staged][mode], seq_lens, qsl, batch, num_heads, max_pages,
-                                     page_size, num_splits, num_clusters, group_rows, plan, w);
+                                     page_size, num_splits, num_clusters, group_rows, plan, w, qa, write_blocks);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -87,3 +87,36 @@ def test_random_configuration_fp8q(seed):
     case = synth.make_decode_case(**kw)
     rows = sample_rows(case, 400, seed=seed) if case.total_q * case.num_heads > 3000 else None
     run_fp8q(case, splits, rows=rows)
+
+
+@pytest.mark.parametrize("num_heads,sq,num_splits", [(128, 1, 0), (16, [1, 3, 2], 2)])
+def test_decode_fp8q_step(num_heads, sq, num_splits):
+    """mla_decode_fp8q_step: its cache rows and query codes equal those of
+    mla_cache_write and mla_quantize_fp8 byte for byte, and its decode meets
+    the e4m3 bar against the oracle on its quantised query."""
+    case = synth.make_decode_case(num_heads=num_heads, batch=3, ctx=(200, 1200), sq=sq, page_size=64,
+                                  cache_dtype="fp8", seed=730 + num_heads, poison=False)
+    qb = q_rows(case)
+    q_scale = float(np.float32(np.abs(oracle.bf16_to_f64(qb)).max() / 448.0))
+    codes = oracle.quantize_fp8(qb, q_scale)
+    ref = GpuCase(case, write_new=False, num_splits_max=num_splits)
+    mla.cache_write(ref.new_kv_c, ref.new_k_pe, ref.slots, ref.cache, case.kv_scale)
+    g = GpuCase(case, write_new=False, num_splits_max=num_splits)
+    q8 = torch.zeros(codes.shape, dtype=torch.uint8, device="cuda")
+    mla.decode_fp8q_step(g.new_kv_c, g.new_k_pe, g.slots, g.q_abs, g.q_pe, q_scale, q8, g.cache, g.block_table,
+                         g.seq_lens, g.out, g.workspace, scale=case.scale, query_start_loc=g.qsl, lse=g.lse,
+                         num_splits=num_splits, kv_scale=case.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.decode_status(g.workspace) == 0
+    assert torch.equal(g.cache.view(torch.uint8), ref.cache.view(torch.uint8))
+    assert np.array_equal(q8.cpu().numpy(), codes)
+    qf = oracle.e4m3_to_f64(codes) * np.float64(np.float32(q_scale))
+    ref_o, ref_lse, _ = oracle.decode(qf, oracle.prepare_cache(case), case.page_size, oracle.CACHE_E4M3,
+                                      case.kv_scale, case.block_table, case.seq_lens, case.query_start_loc,
+                                      case.num_heads, case.scale)
+    out = g.out.float().reshape(-1, LKV).cpu().numpy().astype(np.float64)
+    lse = g.lse.reshape(-1).cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert float(np.max(np.abs(out - ref_o))) <= 6e-2
+    assert (float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0) <= 1e-3
