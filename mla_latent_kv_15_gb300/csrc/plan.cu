@@ -39,8 +39,8 @@ constexpr int kPlanThreads = 256;
 constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many groups
 // Fixed cost of a work unit in tiles of decode time: loading the group's
 // query into tensor memory, refilling the pipeline and the epilogue (a fit of
-// every CTA's end time on the DeepSeek-V3-shaped batch: ~5 us per unit
-// against ~1.3 us per 64-key tile; 3 and 4 measured alike).  Each group is
+// every CTA's end time on the DeepSeek-V3-shaped batch: ~4 us per unit
+// against ~1.2 us per 64-key tile; 3 and 4 measured alike, 5 worse).  Each group is
 // placed on the balanced axis behind this many virtual tiles, so that CTA
 // pairs starting more groups get fewer real tiles.
 constexpr int kUnitCostTiles = 3;
@@ -70,9 +70,10 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int (&sums)[2]
   return incl - v + before;
 }
 
-// floor(a / b) for 0 <= a < 2^24 and 0 < b < 2^24: a float estimate
-// corrected with integer products; an integer division is a long
-// chain of dependent instructions, and the plan is one chain of them.
+// floor(a / b) for a >= 0, b > 0 and a + b < 2^31: a float estimate (within
+// a few units while a < 2^24) corrected with integer products; an integer
+// division is a long chain of dependent instructions, and the plan is one
+// chain of them.
 __device__ __forceinline__ int divf(int a, int b) {
   int q = __float2int_rz(__fdividef((float)a, (float)b));
   while (q * b > a) --q;          // the estimate is within a few units
