@@ -202,6 +202,35 @@ def test_fp8_query_decode_validation_rejects_before_launch(lib):
     assert call(batch=0, total_q=0) == 0
 
 
+def test_step_validation_rejects_before_launch(lib):
+    """mla_decode_step and mla_decode_fp8q_step check the write's and the
+    decode's arguments on the host before anything is launched; with no
+    query rows and no new rows they are no-ops."""
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def step(kv=fake, n_new=4, cache_dtype=0, kv_scale=1.0, num_heads=16, page_size=64, batch=2, total_q=2):
+        return lib.mla_decode_step(kv, fake, fake, n_new, fake, fake, fake, 10, page_size, cache_dtype, kv_scale,
+                                   fake, 4, fake, batch, None, total_q, num_heads, 0.1, 0, fake, None, fake,
+                                   1 << 30, None)
+
+    assert step(n_new=-1) == -1 and b"num_tokens" in lib.mla_last_error()
+    assert step(kv=P((1 << 20) + 4)) == -1 and b"aligned" in lib.mla_last_error()
+    assert step(cache_dtype=1, kv_scale=0.0) == -1 and b"kv_scale" in lib.mla_last_error()
+    assert step(num_heads=0) == -1 and b"num_heads" in lib.mla_last_error()
+    assert step(page_size=48) == -2 and b"page_size" in lib.mla_last_error()
+    assert step(n_new=0, batch=0, total_q=0) == 0
+
+    def step8(q8=fake, q_scale=0.5, n_new=4, batch=2, total_q=2):
+        return lib.mla_decode_fp8q_step(fake, fake, fake, n_new, fake, fake, q_scale, q8, fake, 10, 64, 0.01, fake,
+                                        4, fake, batch, None, total_q, 16, 0.1, 0, fake, None, fake, 1 << 30, None)
+
+    assert step8(q_scale=0.0) == -1 and b"q_scale" in lib.mla_last_error()
+    assert step8(q8=None) == -1 and b"null" in lib.mla_last_error()
+    assert step8(q8=P((1 << 20) + 8)) == -1 and b"aligned" in lib.mla_last_error()
+    assert step8(n_new=0, batch=0, total_q=0) == 0
+
+
 def test_binding_refuses_layouts_the_kernels_would_misread():
     """The kernels read dense rows of fixed element types; the binding refuses
     column slices, transposed views and wrong integer widths before any call
