@@ -120,3 +120,36 @@ def test_decode_fp8q_step(num_heads, sq, num_splits):
     assert np.array_equal(np.isfinite(lse), fin)
     assert float(np.max(np.abs(out - ref_o))) <= 6e-2
     assert (float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0) <= 1e-3
+
+
+def test_decode_fp8q_step_full_size():
+    """The e4m3-query step at the full DeepSeek-V3-shaped size (the query's
+    quantisation blocks stride over 589 824 vectors): every query code equals
+    the oracle's, the cache equals mla_cache_write's, and sampled rows meet the
+    e4m3 bar."""
+    case = synth.workload("dsv3_n128_b64_ctx1k-8k_fp8")
+    qb = q_rows(case)
+    q_scale = float(np.float32(np.abs(oracle.bf16_to_f64(qb)).max() / 448.0))
+    codes = oracle.quantize_fp8(qb, q_scale)
+    g = GpuCase(case, write_new=False)
+    ref_cache = g.cache.clone()
+    mla.cache_write(g.new_kv_c, g.new_k_pe, g.slots, ref_cache, case.kv_scale)
+    q8 = torch.zeros(codes.shape, dtype=torch.uint8, device="cuda")
+    mla.decode_fp8q_step(g.new_kv_c, g.new_k_pe, g.slots, g.q_abs, g.q_pe, q_scale, q8, g.cache, g.block_table,
+                         g.seq_lens, g.out, g.workspace, scale=case.scale, query_start_loc=g.qsl, lse=g.lse,
+                         kv_scale=case.kv_scale)
+    torch.cuda.synchronize()
+    assert mla.decode_status(g.workspace) == 0
+    assert np.array_equal(q8.cpu().numpy(), codes)
+    assert torch.equal(g.cache.view(torch.uint8), ref_cache.view(torch.uint8))
+    rows = sample_rows(case, 300, seed=10)
+    qf = oracle.e4m3_to_f64(codes) * np.float64(np.float32(q_scale))
+    ref_o, ref_lse, _ = oracle.decode(qf, oracle.prepare_cache(case), case.page_size, oracle.CACHE_E4M3,
+                                      case.kv_scale, case.block_table, case.seq_lens, case.query_start_loc,
+                                      case.num_heads, case.scale, rows=rows)
+    out = g.out.float().reshape(-1, LKV).cpu().numpy().astype(np.float64)[rows]
+    lse = g.lse.reshape(-1).cpu().numpy().astype(np.float64)[rows]
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin)
+    assert float(np.max(np.abs(out - ref_o))) <= 6e-2
+    assert (float(np.max(np.abs(lse[fin] - ref_lse[fin]))) if fin.any() else 0.0) <= 1e-3
