@@ -334,9 +334,11 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
   const int write_blocks = writes ? (int)((write->num_tokens + 7) / 8) : 0;
   int quant_blocks = 0;
   if (quant) {
-    // grid-stride: at most two blocks per SM (each holds the plan's shared memory)
+    // grid-stride, the whole launch in one wave: four blocks per SM (each
+    // holds the plan's shared memory), less the plan and write blocks
     const int64_t want = (quant->rows * (kDqk / 8) + kPlanThreads - 1) / kPlanThreads;
-    const int64_t cap = 2LL * (sm_count > 0 ? sm_count : 1);
+    int64_t cap = 4LL * (sm_count > 0 ? sm_count : 1) - 1 - write_blocks;
+    if (cap < (sm_count > 0 ? sm_count : 1)) cap = sm_count > 0 ? sm_count : 1;
     quant_blocks = (int)(want < cap ? (want > 0 ? want : 1) : cap);
   }
   cudaLaunchConfig_t cfg = {};
