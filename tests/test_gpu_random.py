@@ -51,3 +51,26 @@ def test_random_configuration(seed):
         rows = sample_rows(case, 400, seed=seed)
     compare(case, g, rows=rows)
     assert mla.decode_status(g.workspace) == 0
+
+
+@pytest.mark.parametrize("seed", range(100, 116))
+def test_random_configuration_step_sharper(seed):
+    """Drawn configurations through mla_decode_step (the cache write in the
+    plan's launch) with the query times 2^k, k in 1..4 (exact in bf16), so
+    that scores are sharper than the drawn ones."""
+    kw, splits = draw(seed)
+    case = synth.make_decode_case(**kw)
+    k = 1 + seed % 4
+    for name in ("q_abs", "q_pe"):
+        bits = getattr(case, name)
+        f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** k)
+        setattr(case, name, (f.view(np.uint32) >> 16).astype(np.uint16))
+    g = GpuCase(case, write_new=False, num_splits_max=splits)
+    g.out.fill_(float("nan"))
+    mla.decode_step(g.new_kv_c, g.new_k_pe, g.slots, g.q_abs, g.q_pe, g.cache, g.block_table, g.seq_lens, g.out,
+                    g.workspace, scale=case.scale, query_start_loc=g.qsl, lse=g.lse, num_splits=splits,
+                    kv_scale=case.kv_scale)
+    torch.cuda.synchronize()
+    rows = sample_rows(case, 400, seed=seed) if case.total_q * case.num_heads > 3000 else None
+    compare(case, g, rows=rows)
+    assert mla.decode_status(g.workspace) == 0
