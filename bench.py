@@ -96,11 +96,16 @@ def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
-def host_lead(stream, ms: float = 5.0):
-    """Keep the GPU busy (a spin kernel of ~`ms` at the maximum clock) while the
-    host enqueues the timed launches that follow, so that no timed interval
-    includes time the GPU spent waiting for the host to submit work."""
+HOST_US_PER_STEP = 250.0   # host time budgeted per enqueued step (calls, copies, events)
+
+
+def host_lead(stream, steps: int = 0, ms: float = 5.0):
+    """Keep the GPU busy (a spin kernel of ~`ms`, or HOST_US_PER_STEP per step
+    of the `steps` that follow if that is longer, at the maximum clock) while
+    the host enqueues the timed launches that follow, so that no timed
+    interval includes time the GPU spent waiting for the host to submit work."""
     import torch
+    ms = max(ms, steps * HOST_US_PER_STEP / 1000.0)
     with torch.cuda.stream(stream):
         torch.cuda._sleep(int(ms * 2.07e6))
 
@@ -288,7 +293,7 @@ def run_gpu(args):
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        host_lead(stream)
+        host_lead(stream, args.steps)
         if do_flush:
             # the flush between steps stays outside the timed intervals
             for i in range(args.steps):
@@ -305,7 +310,7 @@ def run_gpu(args):
                 step(d)
             ev[0][1].record(stream)
         torch.cuda.synchronize()
-        host_lead(stream)
+        host_lead(stream, args.steps)
         for i in range(args.steps):
             if do_flush:
                 flush.fill_(i & 0xFF)
@@ -399,7 +404,7 @@ def run_gpu(args):
         cs.wait_event(out_done[-1])
 
     torch.cuda.synchronize()
-    host_lead(stream)
+    host_lead(stream, args.steps)
     e2e_start.record(stream)
     run_steps(stream, e2e_start)
     e2e_end.record(stream)
@@ -589,7 +594,7 @@ def run_proj(args):
     t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     with sampler:
-        host_lead(stream)
+        host_lead(stream, args.steps)
         t_a.record(stream)
         for i in range(args.steps):
             op(*sets[i % R])
@@ -692,7 +697,7 @@ def run_gather(args):
     t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
     with sampler:
-        host_lead(stream)
+        host_lead(stream, args.steps)
         t_a.record(stream)
         for _ in range(args.steps):
             op()
