@@ -45,6 +45,34 @@ def test_cache_write_bitexact(dtype, page_size):
     assert np.array_equal(got.reshape(-1), ref.reshape(-1))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_cache_write_skips_slots_past_the_cache(dtype):
+    """Slots at or past num_blocks * page_size are skipped like padding ones
+    (device data is not checked on the host): the cache equals the oracle's
+    write with those tokens marked as padding."""
+    case = synth.make_decode_case(num_heads=4, batch=9, ctx=(1, 300), page_size=64, cache_dtype=dtype, seed=33,
+                                  poison=False)
+    num_slots = case.pool.shape[0] * case.pool.shape[1]
+    slots = case.slot_mapping.copy()
+    past = [1, 4, 7]
+    slots[past] = [num_slots, num_slots + 12345, 1 << 40]
+    g = GpuCase(case, write_new=False)
+    before = g.cache.view(torch.uint8).cpu().numpy().copy()
+    mla.cache_write(g.new_kv_c, g.new_k_pe, torch.from_numpy(slots).cuda(), g.cache, case.kv_scale)
+    torch.cuda.synchronize()
+    got = g.cache.view(torch.uint8).cpu().numpy()
+    pad = slots.copy()
+    pad[past] = -1
+    if dtype == "bf16":
+        ref = before.view(np.uint16).reshape(case.pool.shape).copy()
+        oracle.cache_write(case.new_kv_c, case.new_k_pe, pad, ref, case.page_size, oracle.CACHE_BF16)
+        ref = ref.view(np.uint8)
+    else:
+        ref = before.reshape(case.pool.shape).copy()
+        oracle.cache_write(case.new_kv_c, case.new_k_pe, pad, ref, case.page_size, oracle.CACHE_E4M3, case.kv_scale)
+    assert np.array_equal(got.reshape(-1), ref.reshape(-1))
+
+
 def test_cache_write_preparation_matches_oracle_fp8():
     """The whole fp8 cache the decode tests read (every referenced row
     quantised on the GPU) is bit-identical to the oracle's."""
@@ -248,6 +276,23 @@ def test_block_id_out_of_range_flags_and_does_not_fault():
     g.block_table = bt
     g.decode()
     assert mla.decode_status(g.workspace) & mla.DEVERR_BAD_BLOCK
+
+
+def test_seq_len_beyond_the_block_table_flags_and_clamps():
+    """A request whose seq_len exceeds max_pages * page_size: the scheduler
+    flags DEVERR_BAD_SEQ_LEN and clamps the request to the keys its block
+    table reaches (its unused entries are -1, so they are flagged too and read
+    as zeros), and the other requests keep the oracle's result."""
+    case = synth.make_decode_case(num_heads=32, batch=3, ctx=(300, 900), page_size=64, seed=45, poison=False)
+    g = GpuCase(case)
+    sl = g.seq_lens.clone()
+    sl[1] = case.block_table.shape[1] * case.page_size + 100
+    g.seq_lens = sl
+    g.decode()
+    assert mla.decode_status(g.workspace) & mla.DEVERR_BAD_SEQ_LEN
+    N, qsl = case.num_heads, case.query_start_loc
+    rows = np.array([t * N + h for b in (0, 2) for t in range(qsl[b], qsl[b + 1]) for h in range(N)])
+    compare(case, g, rows=rows)
 
 
 # --------------------------------------------------------- full-size workloads
