@@ -215,6 +215,15 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
             mla::encode_tmap_2d(&tm_kvr, cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, mla::kDqk, kv_rows, mla::kDqk, 32,
                                 kv_box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
+  // the epilogue stores whole 32-row x 64-dim pieces of the output and of the
+  // split partials with TMA (128-B swizzle, as they are staged on chip)
+  const mla::Plan plan = mla::plan_from_workspace(workspace, L);
+  CUtensorMap tm_out, tm_part;
+  enc = enc &&
+        mla::encode_tmap_2d(&tm_out, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, mla::kLkv, rows, mla::kLkv * 2, 64, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B) &&
+        mla::encode_tmap_2d(&tm_part, plan.part_o, CU_TENSOR_MAP_DATA_TYPE_UINT16, mla::kLkv,
+                            (uint64_t)L.max_units * mla::kRows, mla::kLkv * 2, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!enc) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor layout");
 
   mla::DecodeArgs a{};
@@ -243,7 +252,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   a.lse = lse;
   a.wait_limit_ns = g_wait_limit_ns;
   a.debug_skip_tile = g_test_skip_tile;
-  a.plan = mla::plan_from_workspace(workspace, L);
+  a.plan = plan;
 
   cudaStream_t s = (cudaStream_t)stream;
   // small head counts with one query token per request (total_q == batch):
@@ -258,7 +267,7 @@ int decode_impl(const void* q_abs, const void* q_pe, const void* q8, float q_sca
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   const bool timed = g_timing_start && g_timing_stop;
   if (timed && (e = cudaEventRecord(g_timing_start, s)) != cudaSuccess) return cuda_fail(e, "timing event");
-  e = mla::launch_decode(tm_q, tm_qr, tm_kv, tm_kvr, variant, a, clusters, s);
+  e = mla::launch_decode(tm_q, tm_qr, tm_kv, tm_kvr, tm_out, tm_part, variant, a, clusters, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (timed && (e = cudaEventRecord(g_timing_stop, s)) != cudaSuccess) return cuda_fail(e, "timing event");
   e = mla::launch_combine(a, L.max_groups, sms, s);

@@ -174,10 +174,11 @@ cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* qsl, int batch, 
 // maps: the query's latent columns (64-dim boxes; 128-dim e4m3 boxes for
 // variant 3) and its rope columns (32-dim boxes), the cache's latent columns
 // and its rope columns, boxes as wide (rows: min(page, 64) for the cache, 64
-// for the query).
+// for the query); for the epilogue's stores, the bf16 output rows and the
+// fp16 partial rows (64-dim x 32-row boxes, 128-B swizzle).
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
-                          const CUtensorMap& tm_kvr, int variant, const DecodeArgs& a, int num_clusters,
-                          cudaStream_t s);
+                          const CUtensorMap& tm_kvr, const CUtensorMap& tm_out, const CUtensorMap& tm_part,
+                          int variant, const DecodeArgs& a, int num_clusters, cudaStream_t s);
 // sm_count: of the current device (the combine runs one wave of blocks)
 cudaError_t launch_combine(const DecodeArgs& a, int max_groups, int sm_count, cudaStream_t s);
 cudaError_t launch_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,

@@ -373,9 +373,14 @@ template <int kVariant>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
                   const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kvr,
+                  const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_part,
                   const DecodeArgs a) {
   constexpr int kCacheFp8 = kVariant == 1 || kVariant == 3;
   constexpr bool kQ8 = kVariant == 3;       // e4m3 query: fp8 x fp8 score MMAs
+  // the epilogue's pieces leave by TMA stores (bf16 cache, 128-row units:
+  // measured 1 % faster there; the e4m3 variants' softmax warps spill more
+  // with it and the e4m3-query one ran 10 % slower)
+  constexpr bool kTmaStore = kVariant == 0;
   constexpr int kStages = Layout<kVariant>::kStages;
   constexpr int kXBytes = Layout<kVariant>::kXBytes;
   constexpr int kXRows = Layout<kVariant>::kXRows;
@@ -967,6 +972,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       }
       item += 2;
 
+      // the previous unit's TMA stores have read their scratch (receive
+      // buffers the peer may write once this unit's first tiles go out)
+      if constexpr (kTmaStore)
+        if (lane == 0) bulk_wait_group_read<0>();
+
       float m = -INFINITY, l = 0.f;          // l: this half's share of the row sum
       const int ntiles = ur.tile_end - ur.tile_begin;
       // keys of this half of tile jj the row may see (32 on every tile before its last)
@@ -1138,6 +1148,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         }
         __syncwarp();
       };
+      // A warp whose 32 rows all belong to the unit (and every warp writing
+      // split partials, whose slot rows are its own) hands each staged 4 KB
+      // piece to a TMA store and goes on while it drains; the scratch is
+      // written again only once the store has read it (before the next
+      // piece, and before this warp's first send of the next unit: the peer
+      // writes into these buffers only after that).  The 128-row receive
+      // buffers keep the 1024-byte alignment of the 128-B swizzle.
+      static_assert(!kTmaStore || kXRows == kRows, "TMA stores need the 128-row receive buffers");
+      const bool full_rows = q4 * 32 + 32 <= gr.nrows && gr.row0 + q4 * 32 + 32 <= a.total_rows;
+      bool pending = false;
+      auto put = [&](const CUtensorMap* tm, int x, int y) {
+        fence_proxy_async_smem();      // this lane's staged bytes, visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tm, x, y, scr);
+          bulk_commit_group();
+        }
+        pending = true;
+      };
+      auto reclaim = [&]() {
+        if (pending) {
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+          pending = false;
+        }
+      };
       // two 32-column loads of O per wait
 #pragma unroll 1
       for (int cp = 0; cp < 2; ++cp) {
@@ -1146,6 +1182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
         tmem_ld32(tl + kTmemO + 128 * hh + cp * 64 + 32, ob);
         tmem_wait_ld();
         if (!store) continue;
+        reclaim();
         if (ur.slot < 0) {
           // bf16 output: the 64 dims are one 128-byte row piece
 #pragma unroll
@@ -1155,9 +1192,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           for (int v = 0; v < 16; ++v)
             oa[16 + v] = pack_bf16x2(__uint_as_float(ob[2 * v]) * inv, __uint_as_float(ob[2 * v + 1]) * inv);
           stage(oa);
-          drain([&](int r) {
-            return reinterpret_cast<uint8_t*>(out + (size_t)(gr.row0 + q4 * 32 + r) * kLkv + d0 + 64 * cp);
-          });
+          if (kTmaStore && full_rows)
+            put(&tm_out, d0 + 64 * cp, gr.row0 + q4 * 32);
+          else
+            drain([&](int r) {
+              return reinterpret_cast<uint8_t*>(out + (size_t)(gr.row0 + q4 * 32 + r) * kLkv + d0 + 64 * cp);
+            });
         } else if constexpr (kVariant == 2) {
           // partial (see below); one maximum over both halves, the same scale
           // stored for both: this variant's code measured faster in this form
@@ -1203,9 +1243,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
           encode(oa, 0);
           encode(ob, 16);
           stage(oa);
-          drain([&](int r) {
-            return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 + 64 * cp);
-          });
+          if constexpr (kTmaStore)
+            put(&tm_part, d0 + 64 * cp, ur.slot * kRows + q4 * 32);
+          else
+            drain([&](int r) {
+              return reinterpret_cast<uint8_t*>(P.part_o + ((size_t)ur.slot * kRows + q4 * 32 + r) * kLkv + d0 +
+                                                64 * cp);
+            });
         }
       }
       if (valid && rank == 0 && hh == 0) {
@@ -1217,6 +1261,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Roles<kVariant>::kTh
       }
       tc_fence_before();
     }
+    if constexpr (kTmaStore)
+      if (lane == 0) bulk_wait_all();   // every TMA store of the warp is complete
   };
 
   if constexpr (kCacheFp8) {
@@ -1263,8 +1309,8 @@ size_t decode_smem_bytes(int variant) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, const CUtensorMap& tm_kv,
-                          const CUtensorMap& tm_kvr, int variant, const DecodeArgs& a, int num_clusters,
-                          cudaStream_t s) {
+                          const CUtensorMap& tm_kvr, const CUtensorMap& tm_out, const CUtensorMap& tm_part,
+                          int variant, const DecodeArgs& a, int num_clusters, cudaStream_t s) {
   const size_t smem = decode_smem_bytes(variant);
   auto kern = variant == 1 ? decode_kernel<1>
                            : (variant == 2 ? decode_kernel<2> : (variant == 3 ? decode_kernel<3> : decode_kernel<0>));
@@ -1283,7 +1329,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_qr, con
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qr, tm_kv, tm_kvr, a);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_q, tm_qr, tm_kv, tm_kvr, tm_out, tm_part, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -165,6 +165,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
+// TMA store of one 2-d box from shared memory, as a bulk async-group of the
+// issuing thread; the bytes must be made visible to the async proxy first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+// (bulk_commit_group and bulk_wait_group_read below close the group and
+// wait for its source reads)
 // L2 policy: lines loaded under it are the first candidates for eviction
 // (data streamed once, so that it does not push out data read again soon).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -250,6 +260,8 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
+// Wait until every committed bulk group of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // -------------------------------------------------------------------- tcgen05
 
