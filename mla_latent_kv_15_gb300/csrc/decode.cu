@@ -68,7 +68,9 @@
 //    bytes of fp32) and the lse in fp32.  The epilogue stages each warp's
 //    32 rows through 4 KB of shared memory (two receive buffers the peer
 //    cannot be writing at that point) so that its global stores are whole
-//    128-byte lines.
+//    128-byte lines; with a bf16 cache and 128-row units a whole 32-row
+//    piece leaves by one TMA store, which drains while the warp goes on to
+//    the next unit.
 //  * A unit's plan record is one 32-byte line, prefetched into L1 during the
 //    epilogue of the unit before.
 //  * Waits take a completed phase at once and otherwise suspend on the
