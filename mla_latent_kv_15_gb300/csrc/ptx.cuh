@@ -24,20 +24,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.b32 %0, 1, 0, P;\n}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -54,12 +40,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
 
@@ -207,12 +187,6 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
   return r;
 }
 
-__device__ __forceinline__ uint32_t nclusters_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
@@ -243,17 +217,6 @@ __device__ __forceinline__ void st_async_v2(uint32_t remote, uint32_t a, uint32_
                : "memory");
 }
 
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into a
-// peer CTA's shared memory, completing `bytes` of transaction count on the
-// peer's mbarrier.  Both addresses 16-byte aligned.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read their source.
 template <int N>
@@ -364,18 +327,6 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// 32 lanes x 32-bit, 16 consecutive columns: thread i gets row (lane base + i).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
@@ -390,51 +341,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-// 32 lanes x 32-bit, 64 consecutive columns, with the thread's maximum
-// (tmem_ld64_max) or minimum (tmem_ld64_min) of its 64 loaded values as an
+#define MLA_OUTREG(i) "=r"(r[i])
+// 32 lanes x 32-bit, 32 consecutive columns, with the thread's maximum
+// (tmem_ld32_max) or minimum (tmem_ld32_min) of its 32 loaded values as an
 // extra result; the reduction ignores NaN values (sm_103a).
-#define MLA_R64(i) "=r"(r[i])
-#define MLA_TMEM_LD64_RED(NAME, OP)                                                                                    \
-  __device__ __forceinline__ void NAME(uint32_t taddr, uint32_t(&r)[64], float& red) {                                 \
-    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x64." OP                                                          \
-                 ".f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "   \
-                 "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, "     \
-                 "%39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "     \
-                 "%58, %59, %60, %61, %62, %63}, %64, [%65];"                                                          \
-                 : MLA_R64(0), MLA_R64(1), MLA_R64(2), MLA_R64(3), MLA_R64(4), MLA_R64(5), MLA_R64(6), MLA_R64(7),    \
-                   MLA_R64(8), MLA_R64(9), MLA_R64(10), MLA_R64(11), MLA_R64(12), MLA_R64(13), MLA_R64(14),            \
-                   MLA_R64(15), MLA_R64(16), MLA_R64(17), MLA_R64(18), MLA_R64(19), MLA_R64(20), MLA_R64(21),          \
-                   MLA_R64(22), MLA_R64(23), MLA_R64(24), MLA_R64(25), MLA_R64(26), MLA_R64(27), MLA_R64(28),          \
-                   MLA_R64(29), MLA_R64(30), MLA_R64(31), MLA_R64(32), MLA_R64(33), MLA_R64(34), MLA_R64(35),          \
-                   MLA_R64(36), MLA_R64(37), MLA_R64(38), MLA_R64(39), MLA_R64(40), MLA_R64(41), MLA_R64(42),          \
-                   MLA_R64(43), MLA_R64(44), MLA_R64(45), MLA_R64(46), MLA_R64(47), MLA_R64(48), MLA_R64(49),          \
-                   MLA_R64(50), MLA_R64(51), MLA_R64(52), MLA_R64(53), MLA_R64(54), MLA_R64(55), MLA_R64(56),          \
-                   MLA_R64(57), MLA_R64(58), MLA_R64(59), MLA_R64(60), MLA_R64(61), MLA_R64(62), MLA_R64(63),          \
-                   "=f"(red)                                                                                           \
-                 : "r"(taddr)                                                                                          \
-                 : "memory");                                                                                          \
-  }
-MLA_TMEM_LD64_RED(tmem_ld64_max, "max")
-MLA_TMEM_LD64_RED(tmem_ld64_min, "min")
-#undef MLA_TMEM_LD64_RED
-// the same over 32 columns
 #define MLA_TMEM_LD32_RED(NAME, OP)                                                                                    \
   __device__ __forceinline__ void NAME(uint32_t taddr, uint32_t(&r)[32], float& red) {                                 \
     asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x32." OP                                                          \
                  ".f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "   \
                  "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, %32, [%33];"                           \
-                 : MLA_R64(0), MLA_R64(1), MLA_R64(2), MLA_R64(3), MLA_R64(4), MLA_R64(5), MLA_R64(6), MLA_R64(7),    \
-                   MLA_R64(8), MLA_R64(9), MLA_R64(10), MLA_R64(11), MLA_R64(12), MLA_R64(13), MLA_R64(14),            \
-                   MLA_R64(15), MLA_R64(16), MLA_R64(17), MLA_R64(18), MLA_R64(19), MLA_R64(20), MLA_R64(21),          \
-                   MLA_R64(22), MLA_R64(23), MLA_R64(24), MLA_R64(25), MLA_R64(26), MLA_R64(27), MLA_R64(28),          \
-                   MLA_R64(29), MLA_R64(30), MLA_R64(31), "=f"(red)                                                    \
+                 : MLA_OUTREG(0), MLA_OUTREG(1), MLA_OUTREG(2), MLA_OUTREG(3), MLA_OUTREG(4), MLA_OUTREG(5), MLA_OUTREG(6), MLA_OUTREG(7),    \
+                   MLA_OUTREG(8), MLA_OUTREG(9), MLA_OUTREG(10), MLA_OUTREG(11), MLA_OUTREG(12), MLA_OUTREG(13), MLA_OUTREG(14),            \
+                   MLA_OUTREG(15), MLA_OUTREG(16), MLA_OUTREG(17), MLA_OUTREG(18), MLA_OUTREG(19), MLA_OUTREG(20), MLA_OUTREG(21),          \
+                   MLA_OUTREG(22), MLA_OUTREG(23), MLA_OUTREG(24), MLA_OUTREG(25), MLA_OUTREG(26), MLA_OUTREG(27), MLA_OUTREG(28),          \
+                   MLA_OUTREG(29), MLA_OUTREG(30), MLA_OUTREG(31), "=f"(red)                                                    \
                  : "r"(taddr)                                                                                          \
                  : "memory");                                                                                          \
   }
 MLA_TMEM_LD32_RED(tmem_ld32_max, "max")
 MLA_TMEM_LD32_RED(tmem_ld32_min, "min")
 #undef MLA_TMEM_LD32_RED
-#undef MLA_R64
+#undef MLA_OUTREG
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
