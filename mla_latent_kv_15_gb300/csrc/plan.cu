@@ -40,7 +40,7 @@ constexpr int kPlanSmemGroups = 1024;   // staged plans: at most this many group
 // Fixed cost of a work unit in tiles of decode time: loading the group's
 // query into tensor memory, refilling the pipeline and the epilogue (a fit of
 // every CTA's end time on the DeepSeek-V3-shaped batch: ~4 us per unit
-// against ~1.2 us per 64-key tile; 3 and 4 measured alike, 5 worse).  Each group is
+// against ~1.2 us per 64-key tile; 3 and 4 measured alike, 2 and 5 worse).  Each group is
 // placed on the balanced axis behind this many virtual tiles, so that CTA
 // pairs starting more groups get fewer real tiles.
 constexpr int kUnitCostTiles = 3;
